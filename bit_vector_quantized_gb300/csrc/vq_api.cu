@@ -1,0 +1,411 @@
+// vq_api.cu -- the extern "C" boundary (include/vqattn.h): argument checks,
+// launch-shape choice and kernel launches.  No allocation, no synchronisation.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+
+#include "../../include/vqattn.h"
+#include "vq_kernels.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+vq_status fail(vq_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+vq_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(VQ_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int device_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+int device_smem_optin() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+bool decode_formats_supported(const vq_layout& L) {
+  const bool k_ok = (L.k_sub == 2 || L.k_sub == 4) && L.k_bits == 8;
+  const bool v_ok = (L.v_sub == 4 && (L.v_bits == 8 || L.v_bits == 9)) ||
+                    (L.v_sub == 2 && L.v_bits == 8);
+  return k_ok && v_ok;
+}
+
+constexpr int kMaxSplits = 4096;
+
+// Split count minimising an estimate of the persistent grid's makespan:
+// waves(units) * (tokens per unit + fixed per-unit cost).
+int pick_splits(const vq_layout& L, int batch, int max_seq_len, int sms) {
+  const long long pairs = static_cast<long long>(batch) * L.num_kv_heads;
+  const long long chunks = (static_cast<long long>(max_seq_len) + 15) / 16;
+  if (pairs <= 0 || chunks <= 0 || sms <= 0) return 1;
+  const double kUnitOverhead = 384.0;  // tokens-equivalent per unit (q~, merge, pipeline fill)
+  int best = 1;
+  double best_cost = 1e300;
+  const long long smax = std::min<long long>(kMaxSplits, chunks);
+  for (long long s = 1; s <= smax; ++s) {
+    const long long units = pairs * s;
+    if ((units + sms - 1) / sms > vqk::kMaxUnitsPerCta) break;
+    const double waves = static_cast<double>((units + sms - 1) / sms);
+    const double per_unit = std::ceil(static_cast<double>(chunks) / s) * 16.0 + kUnitOverhead;
+    const double cost = waves * per_unit + 8.0 * s;  // combine reads grow with s
+    if (cost < best_cost * 0.999) {
+      best_cost = cost;
+      best = static_cast<int>(s);
+    }
+  }
+  return best;
+}
+
+struct WsLayout {
+  size_t o_off, ml_off, total;
+};
+
+WsLayout ws_layout(const vq_layout& L, int batch, int splits) {
+  WsLayout w;
+  const size_t rows = static_cast<size_t>(batch) * L.num_q_heads * splits;
+  w.o_off = 0;
+  w.ml_off = (rows * L.head_dim * sizeof(float) + 255) & ~size_t(255);
+  w.total = w.ml_off + ((rows * 2 * sizeof(float) + 255) & ~size_t(255));
+  return w;
+}
+
+vq_status check_layout_impl(const vq_layout* L, int for_decode) {
+  if (!L) return fail(VQ_ERR_INVALID_ARG, "layout is NULL");
+  if (!is_pow2(L->head_dim)) return fail(VQ_ERR_INVALID_ARG, "head_dim %d is not a power of two", L->head_dim);
+  if (L->head_dim != 128)
+    return fail(VQ_ERR_UNSUPPORTED, "head_dim %d: this build implements head_dim 128", L->head_dim);
+  if (L->num_q_heads < 1 || L->num_kv_heads < 1 || L->num_q_heads % L->num_kv_heads)
+    return fail(VQ_ERR_INVALID_ARG, "num_q_heads %d must be a positive multiple of num_kv_heads %d",
+                L->num_q_heads, L->num_kv_heads);
+  if (L->num_q_heads / L->num_kv_heads > 8)
+    return fail(VQ_ERR_UNSUPPORTED, "query group %d > 8", L->num_q_heads / L->num_kv_heads);
+  const int subs[2] = {L->k_sub, L->v_sub}, bits[2] = {L->k_bits, L->v_bits};
+  for (int i = 0; i < 2; ++i) {
+    if (!(subs[i] == 1 || subs[i] == 2 || subs[i] == 4 || subs[i] == 8))
+      return fail(VQ_ERR_INVALID_ARG, "%s_sub %d not in {1, 2, 4, 8}", i ? "v" : "k", subs[i]);
+    if (bits[i] < 1 || bits[i] > 12)
+      return fail(VQ_ERR_INVALID_ARG, "%s_bits %d not in 1..12", i ? "v" : "k", bits[i]);
+  }
+  if (L->page_size < 16 || L->page_size % 16)
+    return fail(VQ_ERR_INVALID_ARG, "page_size %d must be a positive multiple of 16", L->page_size);
+  if (for_decode && !decode_formats_supported(*L))
+    return fail(VQ_ERR_UNSUPPORTED,
+                "decode attention implements (k_sub,k_bits) in {(2,8),(4,8)} and (v_sub,v_bits) "
+                "in {(2,8),(4,8),(4,9)}; got (%d,%d) and (%d,%d)",
+                L->k_sub, L->k_bits, L->v_sub, L->v_bits);
+  return VQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t vq_code_row_bytes(int32_t head_dim, int32_t sub, int32_t bits) {
+  if (head_dim <= 0 || sub <= 0 || head_dim % sub || bits < 1 || bits > 16) return 0;
+  const size_t n = static_cast<size_t>(head_dim / sub) * bits;
+  return ((n + 7) / 8 + 3) / 4 * 4;
+}
+
+vq_status vq_check_layout(const vq_layout* layout, int32_t for_decode) {
+  return check_layout_impl(layout, for_decode);
+}
+
+vq_status vq_encode_kv(const vq_layout* layout, int32_t num_tokens, const void* k, const void* v,
+                       const int64_t* slot_mapping, const float* lambda, const void* codebook_k,
+                       const void* codebook_v, void* k_pool, void* v_pool, int64_t num_pages,
+                       int32_t* status, void* stream) {
+  vq_status st = check_layout_impl(layout, 0);
+  if (st != VQ_OK) return st;
+  const vq_layout& L = *layout;
+  if (num_tokens < 0) return fail(VQ_ERR_INVALID_ARG, "num_tokens %d < 0", num_tokens);
+  if (!k && !v) return fail(VQ_ERR_INVALID_ARG, "k and v are both NULL");
+  if (!slot_mapping) return fail(VQ_ERR_INVALID_ARG, "slot_mapping is NULL");
+  if (num_pages < 1) return fail(VQ_ERR_INVALID_ARG, "num_pages %lld < 1", (long long)num_pages);
+  if (k && (!lambda || !codebook_k || !k_pool))
+    return fail(VQ_ERR_INVALID_ARG, "k given but lambda, codebook_k or k_pool is NULL");
+  if (v && (!codebook_v || !v_pool))
+    return fail(VQ_ERR_INVALID_ARG, "v given but codebook_v or v_pool is NULL");
+  const void* ptrs[] = {k, v, lambda, codebook_k, codebook_v, k_pool, v_pool, slot_mapping};
+  for (const void* ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return fail(VQ_ERR_INVALID_ARG, "device buffer %p is not 16-byte aligned", ptr);
+  if (num_tokens == 0) return VQ_OK;
+
+  vqk::EncodeParams p{};
+  p.src[0] = k;
+  p.src[1] = v;
+  p.cb[0] = codebook_k;
+  p.cb[1] = codebook_v;
+  p.pool[0] = static_cast<uint8_t*>(k_pool);
+  p.pool[1] = static_cast<uint8_t*>(v_pool);
+  p.sub[0] = L.k_sub;
+  p.sub[1] = L.v_sub;
+  p.bits[0] = L.k_bits;
+  p.bits[1] = L.v_bits;
+  p.row_bytes[0] = static_cast<int>(vq_code_row_bytes(L.head_dim, L.k_sub, L.k_bits));
+  p.row_bytes[1] = static_cast<int>(vq_code_row_bytes(L.head_dim, L.v_sub, L.v_bits));
+  p.lambda = lambda;
+  p.slots = slot_mapping;
+  p.status = status;
+  p.num_slots = static_cast<long long>(num_pages) * L.page_size;
+  p.num_tokens = num_tokens;
+  p.hkv = L.num_kv_heads;
+  p.page_size = L.page_size;
+  const long long vectors = static_cast<long long>(num_tokens) * L.num_kv_heads;
+  const int sms = device_sms();
+  // few vectors (a decode-step append): spread each codebook scan over 8 warps
+  p.split = vectors * 2 < static_cast<long long>(sms > 0 ? sms : 148) * 8 ? 8 : 1;
+  const int per_cta = 8 / p.split;
+  const long long grid_x = (vectors + per_cta - 1) / per_cta;
+  if (grid_x > 0x7fffffffLL) return fail(VQ_ERR_INVALID_ARG, "too many tokens (%d)", num_tokens);
+  p.which_base = k ? 0 : 1;
+  const int grid_y = (k && v) ? 2 : 1;
+  size_t smem = 0;
+  if (k) smem = std::max(smem, vqk::encode_smem_bytes(L.k_sub, L.k_bits));
+  if (v) smem = std::max(smem, vqk::encode_smem_bytes(L.v_sub, L.v_bits));
+  const int optin = device_smem_optin();
+  if (optin > 0 && smem > static_cast<size_t>(optin))
+    return fail(VQ_ERR_UNSUPPORTED, "encode needs %zu bytes of shared memory, device has %d", smem, optin);
+  cudaError_t e = vqk::launch_encode(p, static_cast<int>(grid_x), grid_y, smem,
+                                     static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "vq_encode_kv launch");
+  return VQ_OK;
+}
+
+int32_t vq_default_num_splits(const vq_layout* layout, int32_t batch, int32_t max_seq_len,
+                              int32_t num_sms) {
+  if (!layout || batch < 0 || max_seq_len < 0 || layout->num_kv_heads < 1) return 0;
+  const int sms = num_sms > 0 ? num_sms : device_sms();
+  if (sms <= 0) return 0;
+  return pick_splits(*layout, batch, max_seq_len, sms);
+}
+
+size_t vq_decode_workspace_bytes(const vq_layout* layout, int32_t batch, int32_t max_seq_len,
+                                 int32_t num_splits, int32_t num_sms) {
+  if (!layout || batch < 0 || max_seq_len < 0 || layout->num_q_heads < 1) return 0;
+  int splits = num_splits;
+  if (splits <= 0) splits = vq_default_num_splits(layout, batch, max_seq_len, num_sms);
+  if (splits <= 0 || splits > kMaxSplits) return 0;
+  return ws_layout(*layout, batch, splits).total;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Validates the decode arguments and fills the split kernel's parameters.
+vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, const float* lambda,
+                         const void* codebook_k, const void* codebook_v, const void* k_pool,
+                         const void* v_pool, int64_t num_pages, const int32_t* page_table,
+                         int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t max_seq_len,
+                         float softmax_scale, int32_t num_splits, const void* workspace,
+                         size_t workspace_bytes, int32_t* status, vqk::DecodeParams& p,
+                         int& grid, size_t& smem) {
+  const vq_layout& L = *layout;
+  const void* ptrs[] = {q, lambda, codebook_k, codebook_v, k_pool, v_pool, page_table, seq_lens, workspace};
+  const char* names[] = {"q", "lambda", "codebook_k", "codebook_v", "k_pool", "v_pool",
+                         "page_table", "seq_lens", "workspace"};
+  for (int i = 0; i < 9; ++i) {
+    if (!ptrs[i]) return fail(VQ_ERR_INVALID_ARG, "%s is NULL", names[i]);
+    if (!aligned16(ptrs[i])) return fail(VQ_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+  }
+  if (num_pages < 1) return fail(VQ_ERR_INVALID_ARG, "num_pages %lld < 1", (long long)num_pages);
+  if (max_pages_per_seq < 1) return fail(VQ_ERR_INVALID_ARG, "max_pages_per_seq %d < 1", max_pages_per_seq);
+  if (max_seq_len < 0) return fail(VQ_ERR_INVALID_ARG, "max_seq_len %d < 0", max_seq_len);
+  if (static_cast<long long>(max_seq_len) > static_cast<long long>(max_pages_per_seq) * L.page_size)
+    return fail(VQ_ERR_INVALID_ARG, "max_seq_len %d exceeds max_pages_per_seq * page_size", max_seq_len);
+  if (!std::isfinite(softmax_scale)) return fail(VQ_ERR_INVALID_ARG, "softmax_scale is not finite");
+  if (num_splits > kMaxSplits) return fail(VQ_ERR_INVALID_ARG, "num_splits %d > %d", num_splits, kMaxSplits);
+
+  const int sms = device_sms();
+  if (sms <= 0) return fail(VQ_ERR_CUDA, "no CUDA device");
+  const int splits = num_splits > 0 ? num_splits : pick_splits(L, batch, max_seq_len, sms);
+  const WsLayout ws = ws_layout(L, batch, splits);
+  if (workspace_bytes < ws.total)
+    return fail(VQ_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, ws.total);
+  const long long units = static_cast<long long>(batch) * L.num_kv_heads * splits;
+  if (units > 0x7fffffffLL) return fail(VQ_ERR_INVALID_ARG, "too many work units");
+  long long g = std::min<long long>(units, sms);
+  g = std::max<long long>(g, (units + vqk::kMaxUnitsPerCta - 1) / vqk::kMaxUnitsPerCta);
+  grid = static_cast<int>(g);
+
+  p = vqk::DecodeParams{};
+  p.q = q;
+  p.lambda = lambda;
+  p.cb_k = codebook_k;
+  p.cb_v = codebook_v;
+  p.k_pool = static_cast<const uint8_t*>(k_pool);
+  p.v_pool = static_cast<const uint8_t*>(v_pool);
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  uint8_t* wsb = static_cast<uint8_t*>(const_cast<void*>(workspace));
+  p.ws_o = reinterpret_cast<float*>(wsb + ws.o_off);
+  p.ws_ml = reinterpret_cast<float2*>(wsb + ws.ml_off);
+  p.status = status;
+  p.num_pages = num_pages;
+  p.timeout_ns = 2000000000ULL;
+  p.batch = batch;
+  p.hq = L.num_q_heads;
+  p.hkv = L.num_kv_heads;
+  p.group = L.num_q_heads / L.num_kv_heads;
+  p.page_size = L.page_size;
+  p.max_pages = max_pages_per_seq;
+  p.max_seq_len = max_seq_len;
+  p.splits = splits;
+  p.num_units = static_cast<int>(units);
+  p.k_row = static_cast<int>(vq_code_row_bytes(L.head_dim, L.k_sub, L.k_bits));
+  p.v_row = static_cast<int>(vq_code_row_bytes(L.head_dim, L.v_sub, L.v_bits));
+  const float scale = softmax_scale == 0.f ? 1.f / std::sqrt(static_cast<float>(L.head_dim)) : softmax_scale;
+  p.qscale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 / std::sqrt(128.0));
+
+  const int optin = device_smem_optin();
+  // consumer shape: 12 warps x 1 chunk for G <= 4, 8 warps x 1 chunk for
+  // G > 4 (register budget); VQ_DECODE_SHAPE=8x1|8x2|12x1 overrides (a tuning
+  // switch for profiling the shapes).
+  vqk::DecodeShape shape = p.group > 4 ? vqk::DecodeShape{8, 1} : vqk::DecodeShape{12, 1};
+  if (const char* env = std::getenv("VQ_DECODE_SHAPE")) {
+    if (std::strcmp(env, "8x2") == 0) shape = vqk::DecodeShape{8, 2};
+    if (std::strcmp(env, "8x1") == 0) shape = vqk::DecodeShape{8, 1};
+    if (std::strcmp(env, "12x1") == 0) shape = vqk::DecodeShape{12, 1};
+  }
+  p.warps = shape.warps;
+  p.chunks = shape.chunks;
+  int nstage = 8;  // pipeline stages: the largest power of two that fits
+  for (; nstage >= 2; nstage /= 2) {
+    smem = vqk::decode_smem(L.k_bits, L.v_bits, p.group, p.k_row, p.v_row, nstage, shape.warps,
+                            shape.stage_tok()).total;
+    if (optin <= 0 || smem <= static_cast<size_t>(optin)) break;
+  }
+  if (nstage < 2) return fail(VQ_ERR_UNSUPPORTED, "decode shared memory does not fit (%zu bytes)", smem);
+  p.nstage = nstage;
+  return VQ_OK;
+}
+
+vq_status launch_partial(const vq_layout& L, const vqk::DecodeParams& p, int grid, size_t smem,
+                         void* stream) {
+  cudaError_t e = vqk::launch_decode(p, L.k_sub, L.k_bits, L.v_sub, L.v_bits, grid, smem,
+                                     static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "decode split kernel");
+  return VQ_OK;
+}
+
+vq_status combine_impl(const vq_layout* layout, int32_t batch, int32_t max_seq_len,
+                       int32_t num_splits, const void* workspace, size_t workspace_bytes,
+                       void* out, void* stream) {
+  const vq_layout& L = *layout;
+  if (!workspace || !out) return fail(VQ_ERR_INVALID_ARG, "workspace or out is NULL");
+  if (!aligned16(workspace) || !aligned16(out))
+    return fail(VQ_ERR_INVALID_ARG, "workspace or out is not 16-byte aligned");
+  if (num_splits > kMaxSplits) return fail(VQ_ERR_INVALID_ARG, "num_splits %d > %d", num_splits, kMaxSplits);
+  int splits = num_splits;
+  if (splits <= 0) {
+    const int sms = device_sms();
+    if (sms <= 0) return fail(VQ_ERR_CUDA, "no CUDA device");
+    splits = pick_splits(L, batch, max_seq_len, sms);
+  }
+  const WsLayout ws = ws_layout(L, batch, splits);
+  if (workspace_bytes < ws.total)
+    return fail(VQ_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, ws.total);
+  vqk::CombineParams cp{};
+  const uint8_t* wsb = static_cast<const uint8_t*>(workspace);
+  cp.ws_o = reinterpret_cast<const float*>(wsb + ws.o_off);
+  cp.ws_ml = reinterpret_cast<const float2*>(wsb + ws.ml_off);
+  cp.out = out;
+  cp.rows = batch * L.num_q_heads;
+  cp.splits = splits;
+  cudaError_t e = vqk::launch_combine(cp, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "decode combine kernel");
+  return VQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+vq_status vq_decode_partial(const vq_layout* layout, int32_t batch, const void* q,
+                            const float* lambda, const void* codebook_k, const void* codebook_v,
+                            const void* k_pool, const void* v_pool, int64_t num_pages,
+                            const int32_t* page_table, int32_t max_pages_per_seq,
+                            const int32_t* seq_lens, int32_t max_seq_len, float softmax_scale,
+                            int32_t num_splits, void* workspace, size_t workspace_bytes,
+                            int32_t* status, void* stream) {
+  vq_status st = check_layout_impl(layout, 1);
+  if (st != VQ_OK) return st;
+  if (batch < 0) return fail(VQ_ERR_INVALID_ARG, "batch %d < 0", batch);
+  if (batch == 0) return VQ_OK;
+  vqk::DecodeParams p;
+  int grid = 0;
+  size_t smem = 0;
+  st = prepare_decode(layout, batch, q, lambda, codebook_k, codebook_v, k_pool, v_pool, num_pages,
+                      page_table, max_pages_per_seq, seq_lens, max_seq_len, softmax_scale,
+                      num_splits, workspace, workspace_bytes, status, p, grid, smem);
+  if (st != VQ_OK) return st;
+  return launch_partial(*layout, p, grid, smem, stream);
+}
+
+vq_status vq_decode_combine(const vq_layout* layout, int32_t batch, int32_t max_seq_len,
+                            int32_t num_splits, const void* workspace, size_t workspace_bytes,
+                            void* out, void* stream) {
+  vq_status st = check_layout_impl(layout, 1);
+  if (st != VQ_OK) return st;
+  if (batch < 0 || max_seq_len < 0) return fail(VQ_ERR_INVALID_ARG, "batch or max_seq_len < 0");
+  if (batch == 0) return VQ_OK;
+  return combine_impl(layout, batch, max_seq_len, num_splits, workspace, workspace_bytes, out, stream);
+}
+
+vq_status vq_decode_attention(const vq_layout* layout, int32_t batch, const void* q,
+                              const float* lambda, const void* codebook_k, const void* codebook_v,
+                              const void* k_pool, const void* v_pool, int64_t num_pages,
+                              const int32_t* page_table, int32_t max_pages_per_seq,
+                              const int32_t* seq_lens, int32_t max_seq_len, float softmax_scale,
+                              int32_t num_splits, void* out, void* workspace,
+                              size_t workspace_bytes, int32_t* status, void* stream) {
+  vq_status st = check_layout_impl(layout, 1);
+  if (st != VQ_OK) return st;
+  if (batch < 0) return fail(VQ_ERR_INVALID_ARG, "batch %d < 0", batch);
+  if (batch == 0) return VQ_OK;
+  if (!out) return fail(VQ_ERR_INVALID_ARG, "out is NULL");
+  if (!aligned16(out)) return fail(VQ_ERR_INVALID_ARG, "out is not 16-byte aligned");
+  vqk::DecodeParams p;
+  int grid = 0;
+  size_t smem = 0;
+  st = prepare_decode(layout, batch, q, lambda, codebook_k, codebook_v, k_pool, v_pool, num_pages,
+                      page_table, max_pages_per_seq, seq_lens, max_seq_len, softmax_scale,
+                      num_splits, workspace, workspace_bytes, status, p, grid, smem);
+  if (st != VQ_OK) return st;
+  st = launch_partial(*layout, p, grid, smem, stream);
+  if (st != VQ_OK) return st;
+  return combine_impl(layout, batch, max_seq_len, p.splits, workspace, workspace_bytes, out, stream);
+}
+
+const char* vq_last_error(void) { return g_last_error.c_str(); }
+
+const char* vq_version(void) { return "vqattn 0.1.0 sm_103a"; }
+
+}  // extern "C"

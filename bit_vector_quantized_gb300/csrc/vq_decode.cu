@@ -1,0 +1,887 @@
+// vq_decode.cu -- split-K fused decode attention over vector-quantized KV codes
+// (sm_103a), and the split-combine kernel.
+//
+// What is computed (VecInfer, section 方法细节 "注意力机制中的向量量化KV缓存"):
+//   q~ = q diag(lambda) H_D,  s = q~ VQ^-1(K~_q, C_k)^T * scale,
+//   p = softmax(s),  o = p VQ^-1(V_q, C_v),
+// one decode query per sequence, query head h reading KV head h / G.  The
+// softmax is evaluated online over tiles with the running-max / running-sum
+// recurrence of the FlashAttention appendix ("相关工作 - FlashAttention"); the
+// sequence is split across CTAs (VecInfer, "细粒度分块计算": a (batch, heads,
+// splits) decomposition) and the split partials are merged by a second kernel
+// with the same recurrence.
+//
+// How it maps to GB300:
+//   * Work unit = (sequence, KV head, split).  A persistent grid of one
+//     8-warp CTA per SM walks its units; each warp walks a contiguous run of
+//     16-token chunks inside each unit.  All G query heads of the KV head are
+//     served by the same CTA, so every code byte is read from HBM once.
+//     Split boundaries depend on max_seq_len only, so the page-table prefetch
+//     never waits for seq_lens; chunks past a sequence's end are skipped.
+//   * Code chunks stream HBM -> shared memory with the TMA bulk-copy engine
+//     (cp.async.bulk, completion on an mbarrier): a private ring of `nstage`
+//     chunk slots per warp, refilled as soon as slots free (VecInfer,
+//     "异步流水线执行": asynchronous prefetch of the next block).  Page numbers
+//     come from a double-buffered 32-entry window per warp, loaded by all lanes
+//     in parallel 32 chunks ahead of use.
+//   * Dequantisation is a gather of fp16 centroids straight into warp-mma
+//     operand registers.  Codebooks stay resident in shared memory, replicated
+//     16x (8-byte centroids) or 32x (4-byte centroids); lane L reads copy L % 16
+//     (L), which places every lane's gather in its own bank pair (bank): gathers
+//     are free of bank conflicts whatever the codes.
+//   * Both contractions run on the tensor pipe with m16n8k16 fp16 mma, fp32
+//     accumulation.  Scores: s^T[16 tok x 8] = K^[16 tok x 128] q~^T; values:
+//     o^T[128 x 8] += V^^T[128 x 16 tok] P^T[16 tok x 8].  Because q~ and p are
+//     rounded to fp16 operands, each is split into hi + lo fp16 parts: with
+//     G <= 4 the hi and lo parts occupy the otherwise empty columns 2g and 2g+1
+//     of the 8-wide operand (no extra mma); with 4 < G <= 8 hi and lo take one
+//     mma each.  Centroids are exact fp16 values, so the products keep about
+//     fp32 accuracy.
+//   * The K and V feature dimensions are permuted consistently (a dot product
+//     and an output row set do not depend on the order) so that each lane's
+//     operand registers are exactly one centroid gather: the lane with
+//     (lane % 4) = c holds dims 32c + 4k .. 32c + 4k + 3 of k-step k for K, and
+//     the lane with lane / 4 = r accumulates output dims 16r .. 16r + 15 for V.
+//   * Each warp iteration processes two 16-token chunks, so the two mma chains,
+//     their gathers and the softmax bookkeeping overlap.
+#include <type_traits>
+
+#include "vq_device.cuh"
+#include "vq_kernels.h"
+
+namespace vqk {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Shared-memory gathers from the read-only codebook replicas (32-bit addresses).
+__device__ __forceinline__ uint2 gather64(uint32_t a) {
+  uint2 v;
+  asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t gather32(uint32_t a) {
+  uint32_t v;
+  asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// Byte i of w, scaled by the 128-byte replica row stride.
+__device__ __forceinline__ uint32_t row_of_byte(uint32_t w, int i) {
+  return __byte_perm(w, 0, 0x4440 | i) << 7;
+}
+
+// K codes of one token for the lane's 8 (dk = 4) or 16 (dk = 2) sub-vectors.
+template <int DK>
+struct KCodes;
+template <>
+struct KCodes<4> {
+  uint2 w;
+  __device__ __forceinline__ void load(const uint8_t* row, int c) {
+    w = *reinterpret_cast<const uint2*>(row + 8 * c);
+  }
+  __device__ __forceinline__ uint32_t off(int i) const { return row_of_byte(i < 4 ? w.x : w.y, i & 3); }
+};
+template <>
+struct KCodes<2> {
+  uint4 w;
+  __device__ __forceinline__ void load(const uint8_t* row, int c) {
+    w = *reinterpret_cast<const uint4*>(row + 16 * c);
+  }
+  __device__ __forceinline__ uint32_t off(int i) const {
+    const uint32_t v = i < 4 ? w.x : i < 8 ? w.y : i < 12 ? w.z : w.w;
+    return row_of_byte(v, i & 3);
+  }
+};
+
+// V codes of one token for the lane's sub-vectors: dv = 4 -> sub-vectors
+// 4r .. 4r+3 (8- or 9-bit codes), dv = 2 -> sub-vectors 8r .. 8r+7 (8-bit).
+template <int DV, int BV>
+struct VCodes;
+template <>
+struct VCodes<4, 8> {
+  uint32_t w;
+  __device__ __forceinline__ void load(const uint8_t* row, int r) {
+    w = *reinterpret_cast<const uint32_t*>(row + 4 * r);
+  }
+  __device__ __forceinline__ uint32_t off(int i) const { return row_of_byte(w, i); }
+};
+template <>
+struct VCodes<4, 9> {
+  uint32_t lo, hi;
+  int sh;
+  __device__ __forceinline__ void load(const uint8_t* row, int r) {
+    // codes 4r .. 4r+3 sit at bits 36r .. 36r+35: words r and r+1, shift 4r
+    lo = *reinterpret_cast<const uint32_t*>(row + 4 * r);
+    hi = *reinterpret_cast<const uint32_t*>(row + 4 * r + 4);
+    sh = 4 * r;
+  }
+  __device__ __forceinline__ uint32_t off(int i) const {
+    const uint64_t w = (static_cast<uint64_t>(hi) << 32) | lo;
+    return (static_cast<uint32_t>(w >> (sh + 9 * i)) & 0x1ffu) << 7;
+  }
+};
+template <>
+struct VCodes<2, 8> {
+  uint2 w;
+  __device__ __forceinline__ void load(const uint8_t* row, int r) {
+    w = *reinterpret_cast<const uint2*>(row + 8 * r);
+  }
+  __device__ __forceinline__ uint32_t off(int i) const { return row_of_byte(i < 4 ? w.x : w.y, i & 3); }
+};
+
+struct UnitId {
+  int b, kvh, s;
+};
+
+__device__ __forceinline__ UnitId unit_id(const DecodeParams& p, int k) {
+  const int u = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+  UnitId id;
+  id.s = u % p.splits;
+  const int bk = u / p.splits;
+  id.kvh = bk % p.hkv;
+  id.b = bk / p.hkv;
+  return id;
+}
+
+// Barrier among the NP producer warps only (id 2).
+template <int NP>
+__device__ __forceinline__ void producer_sync() {
+  asm volatile("bar.sync 2, %0;" ::"n"(NP * 32) : "memory");
+}
+
+// Barrier among the NW consumer warps only (id 1; the producer warps run ahead).
+template <int NW>
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory");
+}
+
+// Pipeline stages of one work unit.  A unit covers 32-token blocks [a, b) of
+// its sequence (split boundaries from max_seq_len), clipped to the sequence
+// length; stage j holds its tokens [t0, tend) with t0 = 32 a + 256 j.
+struct UnitStages {
+  int b, kvh, s, len, t_begin, t_end, count;
+};
+
+template <int kStageTok>
+__device__ __forceinline__ UnitStages unit_stages(const DecodeParams& p, int k, int len) {
+  const UnitId id = unit_id(p, k);
+  const int nsl = (p.max_seq_len + kUnitTok - 1) / kUnitTok;
+  const int a = static_cast<int>(static_cast<long long>(id.s) * nsl / p.splits);
+  const int b = static_cast<int>(static_cast<long long>(id.s + 1) * nsl / p.splits);
+  UnitStages u;
+  u.b = id.b;
+  u.kvh = id.kvh;
+  u.s = id.s;
+  u.len = len;
+  u.t_begin = a * kUnitTok;
+  u.t_end = min(b * kUnitTok, len);
+  u.count = u.t_end > u.t_begin ? (u.t_end - u.t_begin + kStageTok - 1) / kStageTok : 0;
+  return u;
+}
+
+template <int DK, int BK, int DV, int BV, int NG, int NW, int kNCH>
+__global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split_kernel(const DecodeParams p) {
+  static_assert(BK == 8, "K codes are byte-aligned in this build");
+  static_assert(NG == 4 || NG == 8, "query heads per pass");
+  static_assert(kNCH == 1 || kNCH == 2, "chunks per consumer warp");
+  constexpr int NGL = NG == 4 ? 1 : 2;       // heads owned by one lane
+  constexpr int NP = kProducerWarps;
+  constexpr int kSlice = kNCH * kChunk;      // tokens per consumer warp per stage
+  constexpr int kStageTok = NW * kSlice;     // tokens per pipeline stage
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int G = p.group;
+  const int NS = p.nstage;  // power of two
+  const DecodeSmem L = decode_smem(BK, BV, G, p.k_row, p.v_row, NS, NW, kStageTok);
+  float* qt = reinterpret_cast<float*>(smem + L.qt);
+  float* merge = reinterpret_cast<float*>(smem + L.merge);
+  float2* mlbuf = reinterpret_cast<float2*>(smem + L.ml);
+  int* ulen_c = reinterpret_cast<int*>(smem + L.units);  // unit lengths, consumers' copy
+  int* ulen_p = ulen_c + kMaxUnitsPerCta;                  // producers' copy
+  int4* meta = reinterpret_cast<int4*>(smem + L.meta);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar);
+  uint64_t* empty = full + NS;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flag);
+  uint8_t* stages = smem + L.stage;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int stage_bytes = kStageTok * (p.k_row + p.v_row);
+  const int ns_shift = __ffs(NS) - 1;
+  const int n_units = (p.num_units - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                      static_cast<int>(gridDim.x);
+  auto clamp_len = [&](int len) { return len < 0 ? 0 : (len > p.max_seq_len ? p.max_seq_len : len); };
+
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, NW);
+    }
+    mbar_init_fence();
+    *abort_flag = 0;
+  }
+  __syncthreads();  // barriers initialised; producers and consumers now run independently
+
+  if (warp >= NW) {
+    // =========================== producer warps ==============================
+    // Producer warp pw = warp - NW owns stages n = pw, pw + NP, pw + 2 NP, ...;
+    // stage n goes to slot n % NS.  The stage's K rows and V rows are cut into
+    // pieces of at most ~4 KB on a token grid that divides the page size (a
+    // piece never crosses a page); lane i looks up the page of piece i and,
+    // after lane 0 has armed the slot's full barrier with the byte count,
+    // issues that piece as one bulk copy.  A warp issuing bulk copies stalls
+    // while the copy engine accepts them, so several producer warps together
+    // keep enough bytes in flight to reach HBM bandwidth.
+    const int pw = warp - NW;
+    for (int k = tid - NW * 32; k < n_units; k += NP * 32)
+      ulen_p[k] = clamp_len(__ldg(p.seq_lens + unit_id(p, k).b));
+    producer_sync<NP>();
+    const int P = p.page_size;
+    auto piece_tok = [&](int row) {  // largest 16 * 2^i dividing P with <= 4 KB
+      int t = kChunk;
+      while (t * 2 <= P && P % (t * 2) == 0 && t * 2 * row <= 4096) t *= 2;
+      return t;
+    };
+    const int lk = __ffs(piece_tok(p.k_row)) - 1, lv = __ffs(piece_tok(p.v_row)) - 1;
+    struct It {  // stage iterator over (unit k, stage j), skipping empty units
+      int k, j;
+      UnitStages u;
+    };
+    auto it_seek = [&](It& it) {
+      while (it.k < n_units && it.j >= it.u.count) {
+        ++it.k;
+        it.j = 0;
+        if (it.k < n_units) it.u = unit_stages<kStageTok>(p, it.k, ulen_p[it.k]);
+      }
+    };
+    auto skip = [&](It& it) {  // advance by NP stages
+      for (int i = 0; i < NP && it.k < n_units; ++i) {
+        ++it.j;
+        it_seek(it);
+      }
+    };
+    struct Piece {  // this lane's piece of a stage: tensor (0 = K, 1 = V), tokens
+      int which, t_lo, t_hi;
+    };
+    auto piece_of = [&](const UnitStages& su, int sj) -> Piece {
+      const int t0 = su.t_begin + sj * kStageTok;
+      const int tend16 = (min(t0 + kStageTok, su.t_end) + kChunk - 1) & ~(kChunk - 1);
+      const int nk = ((tend16 - 1) >> lk) - (t0 >> lk) + 1;
+      Piece pc;
+      pc.which = lane < nk ? 0 : 1;
+      const int l2 = pc.which == 0 ? lk : lv;
+      const int idx = (t0 >> l2) + (pc.which == 0 ? lane : lane - nk);
+      pc.t_lo = max(t0, idx << l2);
+      pc.t_hi = min(tend16, (idx + 1) << l2);
+      return pc;
+    };
+    auto lookup = [&](const It& it) -> int {  // page of this lane's piece of stage `it`
+      if (it.k >= n_units) return -1;
+      const Piece pc = piece_of(it.u, it.j);
+      if (pc.t_lo >= pc.t_hi) return -1;
+      const int pi = pc.t_lo / P;
+      return pi < p.max_pages ? __ldg(p.page_table + static_cast<long long>(it.u.b) * p.max_pages + pi) : -1;
+    };
+    auto issue = [&](const UnitStages& su, int sj, int page, int n) {
+      const int slot = n & (NS - 1);
+      const int t0 = su.t_begin + sj * kStageTok;
+      const int tend = min(t0 + kStageTok, su.t_end);
+      const Piece pc = piece_of(su, sj);
+      const bool has = pc.t_lo < pc.t_hi;
+      const bool ok = has && page >= 0 && page < p.num_pages;
+      if (has && !ok) report(p.status, kDevBadPage);
+      const int row = pc.which == 0 ? p.k_row : p.v_row;
+      const uint32_t bytes = ok ? static_cast<uint32_t>(pc.t_hi - pc.t_lo) * row : 0u;
+      uint32_t mask = 0;  // 16-token chunks with data (from the K pieces)
+      if (ok && pc.which == 0) {
+        const int c0 = (pc.t_lo - t0) / kChunk, c1 = (pc.t_hi - t0) / kChunk;
+        mask = ((1u << c1) - 1u) & ~((1u << c0) - 1u);
+      }
+      const uint32_t total = __reduce_add_sync(kFull, bytes);
+      const uint32_t vmask = __reduce_or_sync(kFull, mask);
+      if (lane == 0) {
+        meta[slot] = make_int4(t0, tend, static_cast<int>(vmask), 0);
+        if (total) mbar_arrive_expect_tx(full + slot, total);
+        else mbar_arrive(full + slot);
+      }
+      __syncwarp();
+      if (ok) {
+        uint8_t* dst = stages + static_cast<size_t>(slot) * stage_bytes +
+                       (pc.which == 0 ? 0 : kStageTok * p.k_row) + (pc.t_lo - t0) * row;
+        const uint8_t* pool = pc.which == 0 ? p.k_pool : p.v_pool;
+        const long long row0 = (static_cast<long long>(page) * p.hkv + su.kvh) * P + (pc.t_lo % P);
+        bulk_copy_g2s(dst, pool + row0 * row, (pc.t_hi - pc.t_lo) * row, full + slot);
+      }
+    };
+    // Page numbers run 4 of this warp's stages ahead of its copies: ring[i]
+    // holds the pages of its next stage with index % 4 == i.
+    It cur;
+    cur.k = 0;
+    cur.j = 0;
+    if (n_units > 0) cur.u = unit_stages<kStageTok>(p, 0, ulen_p[0]);
+    it_seek(cur);
+    for (int i = 0; i < pw && cur.k < n_units; ++i) {
+      ++cur.j;
+      it_seek(cur);
+    }
+    It ahead = cur;
+    int ring[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      ring[i] = lookup(ahead);
+      skip(ahead);
+    }
+    int n = pw;
+    bool stop = false;
+    while (cur.k < n_units && !stop) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (cur.k >= n_units || stop) break;
+        const int slot = n & (NS - 1);
+        if (n >= NS) {  // wait until the consumers have released the slot
+          const uint32_t par = static_cast<uint32_t>((n >> ns_shift) - 1) & 1u;
+          bool ok = !*abort_flag && mbar_wait_bounded(empty + slot, par, abort_flag, p.timeout_ns);
+          ok = __all_sync(kFull, ok);
+          if (!ok) {
+            if (lane == 0 && !*abort_flag) {
+              *abort_flag = 1;
+              report(p.status, kDevTimeout);
+            }
+            stop = true;
+            break;
+          }
+        }
+        issue(cur.u, cur.j, ring[i], n);
+        ring[i] = lookup(ahead);
+        skip(ahead);
+        n += NP;
+        skip(cur);
+      }
+    }
+    __syncthreads();  // every consumer is done
+    if (*abort_flag && lane == 0) {  // wait (bounded) for this warp's copies still in flight
+      for (int i = n - NP; i >= 0 && i >= n - NS - NP; i -= NP) {
+        volatile int no_abort = 0;
+        mbar_wait_bounded(full + (i & (NS - 1)), static_cast<uint32_t>(i >> ns_shift) & 1u, &no_abort,
+                          p.timeout_ns);
+      }
+    }
+    return;
+  }
+
+  // ============================= consumer warps ==============================
+  constexpr int kConsumerThreads = NW * 32;
+  constexpr int kNK = ((1 << BK) + kConsumerThreads - 1) / kConsumerThreads;
+  constexpr int kNV = ((1 << BV) + kConsumerThreads - 1) / kConsumerThreads;
+  uint2 cbk_r[kNK], cbv_r[kNV];
+#pragma unroll
+  for (int i = 0; i < kNK; ++i) {
+    const int j = tid + i * kConsumerThreads;
+    if (j < (1 << BK)) {
+      if constexpr (DK == 4) cbk_r[i] = __ldg(reinterpret_cast<const uint2*>(p.cb_k) + j);
+      else cbk_r[i].x = __ldg(reinterpret_cast<const uint32_t*>(p.cb_k) + j);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kNV; ++i) {
+    const int j = tid + i * kConsumerThreads;
+    if (j < (1 << BV)) {
+      if constexpr (DV == 4) cbv_r[i] = __ldg(reinterpret_cast<const uint2*>(p.cb_v) + j);
+      else cbv_r[i].x = __ldg(reinterpret_cast<const uint32_t*>(p.cb_v) + j);
+    }
+  }
+  int len_r = 0;
+  if (tid < n_units) len_r = __ldg(p.seq_lens + unit_id(p, tid).b);
+  uint2 q_r = make_uint2(0, 0);
+  float4 lam_r = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto load_q = [&](int k) {  // query and lambda of unit k (consumer warps < G)
+    if (warp < G && k < n_units) {
+      const UnitId id = unit_id(p, k);
+      q_r = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.q) +
+                                               (static_cast<long long>(id.b) * p.hq + id.kvh * G + warp) * kHeadDim) +
+                  lane);
+      lam_r = __ldg(reinterpret_cast<const float4*>(p.lambda + id.kvh * kHeadDim) + lane);
+    }
+  };
+  load_q(0);
+  {  // codebook replicas: 8-byte centroid j -> 16 copies at j*128 + copy*8; 4-byte -> 32 at j*128 + copy*4
+    const uint32_t cbk = smem_addr(smem + L.cbk), cbv = smem_addr(smem + L.cbv);
+#pragma unroll
+    for (int i = 0; i < kNK; ++i) {
+      const int j = tid + i * kConsumerThreads;
+      if (j < (1 << BK)) {
+        if constexpr (DK == 4) {
+#pragma unroll
+          for (int rep = 0; rep < 16; ++rep)
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(cbk + j * 128 + rep * 8),
+                         "r"(cbk_r[i].x), "r"(cbk_r[i].y));
+        } else {
+#pragma unroll
+          for (int rep = 0; rep < 32; ++rep)
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(cbk + j * 128 + rep * 4), "r"(cbk_r[i].x));
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kNV; ++i) {
+      const int j = tid + i * kConsumerThreads;
+      if (j < (1 << BV)) {
+        if constexpr (DV == 4) {
+#pragma unroll
+          for (int rep = 0; rep < 16; ++rep)
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(cbv + j * 128 + rep * 8),
+                         "r"(cbv_r[i].x), "r"(cbv_r[i].y));
+        } else {
+#pragma unroll
+          for (int rep = 0; rep < 32; ++rep)
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(cbv + j * 128 + rep * 4), "r"(cbv_r[i].x));
+        }
+      }
+    }
+  }
+  if (tid < n_units) ulen_c[tid] = clamp_len(len_r);
+  consumer_sync<NW>();  // codebooks and unit lengths visible to the consumers
+
+  const int r = lane >> 2, c = lane & 3;
+  const uint32_t cbk_lane = smem_addr(smem + L.cbk) + (DK == 4 ? (lane & 15) * 8 : lane * 4);
+  const uint32_t cbv_lane = smem_addr(smem + L.cbv) + (DV == 4 ? (lane & 15) * 8 : lane * 4);
+  uint32_t qa[8][2];  // score B operands: NG == 4: columns (2g: hi, 2g+1: lo); NG == 8: hi
+  uint32_t qb[8][2];  // NG == 8: lo
+  float O[8][4];      // output accumulators (NG == 4 uses O[0..3])
+  float m_run[NGL], l_run[NGL];
+
+  // ---- code registers -------------------------------------------------------
+  // K: tokens r and r+8 of a chunk.  V (G <= 4): tokens c, c+4, c+8, c+12;
+  // V (G > 4): tokens 2c, 2c+1, 2c+8, 2c+9, and with 32-byte rows lanes c >= 2
+  // read each pair swapped so that every load hits 32 different banks (the
+  // PRMT selectors undo the swap).
+  constexpr bool kSwap = NG == 8 && DV == 4 && BV == 8;
+  const int sw = (kSwap && c >= 2) ? 1 : 0;
+  const uint32_t sel_lo = sw ? 0x1054u : 0x5410u, sel_hi = sw ? 0x3276u : 0x7632u;
+  KCodes<DK> kc[kNCH][2];          // current stage
+  VCodes<DV, BV> vc[kNCH][4];      // current stage
+  VCodes<DV, BV> pvc[kNCH][4];     // previous stage, P.V pending
+  uint32_t pb[kNCH][2][2];         // previous stage's P operands [chunk][k-step or token pair][reg]
+
+  auto load_codes = [&](const uint8_t* st, int off) {
+#pragma unroll
+    for (int n = 0; n < kNCH; ++n) {
+      kc[n][0].load(st + (off + n * kChunk + r) * p.k_row, c);
+      kc[n][1].load(st + (off + n * kChunk + r + 8) * p.k_row, c);
+      const uint8_t* sv = st + kStageTok * p.k_row + (off + n * kChunk) * p.v_row;
+      if constexpr (NG == 4) {
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) vc[n][jj].load(sv + (c + 4 * jj) * p.v_row, r);
+      } else {
+        const uint8_t* vr0 = sv + (2 * c) * p.v_row;
+        vc[n][0].load(vr0 + sw * p.v_row, r);
+        vc[n][1].load(vr0 + (1 - sw) * p.v_row, r);
+        vc[n][2].load(vr0 + (8 + sw) * p.v_row, r);
+        vc[n][3].load(vr0 + (9 - sw) * p.v_row, r);
+      }
+    }
+  };
+
+  // P.V of the previous stage's chunks, output step q (0..3 for G <= 4).
+  //  G <= 4: the mma reduction index runs over (token t', element e) with
+  //    k = 2 t' + e, so one gathered fp16 pair of a centroid is one operand
+  //    register; the output column (2g + e') selects element e' of head g.
+  //    Output rows r, r+8 of step q are the element pairs 0 and 1 (dv = 4) or
+  //    sub-vectors 8r + 2q, 8r + 2q + 1 (dv = 2); lane (r, c) accumulates dims
+  //    16r + 4q .. 16r + 4q + 3 of head c.
+  //  G > 4: reduction over 16 tokens, A = V^T built with PRMT (pairs of tokens).
+  auto pv_step = [&](int q) {
+#pragma unroll
+    for (int n = 0; n < kNCH; ++n) {
+      if constexpr (NG == 4) {
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {  // tokens 8ks + c and 8ks + c + 4
+          uint32_t a0, a1, a2, a3;
+          if constexpr (DV == 4) {
+            const uint2 w0 = gather64(cbv_lane + pvc[n][2 * ks].off(q));
+            const uint2 w1 = gather64(cbv_lane + pvc[n][2 * ks + 1].off(q));
+            a0 = w0.x; a1 = w0.y; a2 = w1.x; a3 = w1.y;
+          } else {
+            a0 = gather32(cbv_lane + pvc[n][2 * ks].off(2 * q));
+            a1 = gather32(cbv_lane + pvc[n][2 * ks].off(2 * q + 1));
+            a2 = gather32(cbv_lane + pvc[n][2 * ks + 1].off(2 * q));
+            a3 = gather32(cbv_lane + pvc[n][2 * ks + 1].off(2 * q + 1));
+          }
+          mma16816(O[q], a0, a1, a2, a3, pb[n][ks][0], pb[n][ks][1]);
+        }
+      } else {
+        if constexpr (DV == 4) {  // q = output step pair (2q, 2q+1)
+          uint2 W[4];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) W[jj] = gather64(cbv_lane + pvc[n][jj].off(q));
+          mma16816(O[2 * q], __byte_perm(W[0].x, W[1].x, sel_lo), __byte_perm(W[0].x, W[1].x, sel_hi),
+                   __byte_perm(W[2].x, W[3].x, sel_lo), __byte_perm(W[2].x, W[3].x, sel_hi), pb[n][0][0],
+                   pb[n][0][1]);
+          mma16816(O[2 * q + 1], __byte_perm(W[0].y, W[1].y, sel_lo), __byte_perm(W[0].y, W[1].y, sel_hi),
+                   __byte_perm(W[2].y, W[3].y, sel_lo), __byte_perm(W[2].y, W[3].y, sel_hi), pb[n][0][0],
+                   pb[n][0][1]);
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t W[4];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) W[jj] = gather32(cbv_lane + pvc[n][jj].off(2 * q + h));
+            mma16816(O[2 * q + h], __byte_perm(W[0], W[1], 0x5410), __byte_perm(W[0], W[1], 0x7632),
+                     __byte_perm(W[2], W[3], 0x5410), __byte_perm(W[2], W[3], 0x7632), pb[n][0][0],
+                     pb[n][0][1]);
+          }
+        }
+      }
+    }
+  };
+
+  // One basic block: scores of the current chunks and P.V of the previous
+  // chunks, two independent streams the scheduler interleaves.
+  auto fused = [&](float (&sc)[kNCH][4], bool with_qk) {
+    float acc[kNCH][2][4], acc2[kNCH][2][4];  // [chunk][k-step parity][..]
+#pragma unroll
+    for (int n = 0; n < kNCH; ++n)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) acc[n][e][jj] = acc2[n][e][jj] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      if (with_qk) {
+#pragma unroll
+        for (int n = 0; n < kNCH; ++n) {
+          uint32_t a0, a1, a2, a3;
+          if constexpr (DK == 4) {
+            const uint2 g0 = gather64(cbk_lane + kc[n][0].off(kk));
+            const uint2 g1 = gather64(cbk_lane + kc[n][1].off(kk));
+            a0 = g0.x; a1 = g1.x; a2 = g0.y; a3 = g1.y;
+          } else {
+            a0 = gather32(cbk_lane + kc[n][0].off(2 * kk));
+            a1 = gather32(cbk_lane + kc[n][1].off(2 * kk));
+            a2 = gather32(cbk_lane + kc[n][0].off(2 * kk + 1));
+            a3 = gather32(cbk_lane + kc[n][1].off(2 * kk + 1));
+          }
+          mma16816(acc[n][kk & 1], a0, a1, a2, a3, qa[kk][0], qa[kk][1]);
+          if constexpr (NG == 8) mma16816(acc2[n][kk & 1], a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        }
+      }
+      if ((kk & 1) == 0) pv_step(kk >> 1);
+    }
+#pragma unroll
+    for (int n = 0; n < kNCH; ++n)
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        sc[n][jj] = acc[n][0][jj] + acc[n][1][jj];
+        if constexpr (NG == 8) sc[n][jj] += acc2[n][0][jj] + acc2[n][1][jj];
+      }
+  };
+
+  // Online softmax (log2 domain) over the current chunks: updates m and l,
+  // rescales O, and leaves the chunks' P operands (fp16) in pb.  Tokens at or
+  // past `lim`, and chunks whose bit in `live` is clear, get p = 0.
+  auto softmax = [&](const float (&sc)[kNCH][4], int tok0, int lim, uint32_t live) {
+    float s[kNCH][NGL][2];
+#pragma unroll
+    for (int n = 0; n < kNCH; ++n) {
+      const int t0 = tok0 + n * kChunk + r, t1 = t0 + 8;
+      const int lim_n = ((live >> n) & 1u) ? lim : 0;
+      if constexpr (NG == 4) {  // columns 2c (hi) + 2c+1 (lo) of head c
+        s[n][0][0] = t0 < lim_n ? sc[n][0] + sc[n][1] : -INFINITY;
+        s[n][0][1] = t1 < lim_n ? sc[n][2] + sc[n][3] : -INFINITY;
+      } else {                  // columns 2c, 2c+1 = heads 2c, 2c+1
+        s[n][0][0] = t0 < lim_n ? sc[n][0] : -INFINITY;
+        s[n][1][0] = t0 < lim_n ? sc[n][1] : -INFINITY;
+        s[n][0][1] = t1 < lim_n ? sc[n][2] : -INFINITY;
+        s[n][1][1] = t1 < lim_n ? sc[n][3] : -INFINITY;
+      }
+    }
+    float alpha[NGL];
+    bool rescale = false;
+#pragma unroll
+    for (int gi = 0; gi < NGL; ++gi) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int n = 0; n < kNCH; ++n) mx = fmaxf(mx, fmaxf(s[n][gi][0], s[n][gi][1]));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+      const float mnew = fmaxf(m_run[gi], mx);
+      const float mref = mnew == -INFINITY ? 0.f : mnew;
+      alpha[gi] = fast_exp2(m_run[gi] - mref);
+      rescale = rescale || alpha[gi] != 1.f;
+      float lsum = 0.f;
+#pragma unroll
+      for (int n = 0; n < kNCH; ++n)
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          s[n][gi][t] = fast_exp2(s[n][gi][t] - mref);
+          lsum += s[n][gi][t];
+        }
+      l_run[gi] = l_run[gi] * alpha[gi] + lsum;
+      m_run[gi] = mnew;
+    }
+    if (__any_sync(kFull, rescale)) {
+      if constexpr (NG == 4) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) O[i][jj] *= alpha[0];
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          O[i][0] *= alpha[0]; O[i][2] *= alpha[0];
+          O[i][1] *= alpha[NGL - 1]; O[i][3] *= alpha[NGL - 1];
+        }
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < kNCH; ++n) {
+      if constexpr (NG == 4) {
+        // B[k = 2t' + e][col = 2g + e'] = p[t'][g] * (e == e'): lane (r, c) needs
+        // p of head r/2 for tokens c, c+4 (k-step 0) and c+8, c+12 (k-step 1),
+        // held by lanes 4c + r/2 and 4(c+4) + r/2 (rows r and r+8 of the chunk).
+        const int src0 = 4 * c + (r >> 1), src1 = 4 * (c + 4) + (r >> 1);
+        const float p00 = __shfl_sync(kFull, s[n][0][0], src0), p01 = __shfl_sync(kFull, s[n][0][0], src1);
+        const float p10 = __shfl_sync(kFull, s[n][0][1], src0), p11 = __shfl_sync(kFull, s[n][0][1], src1);
+        const int sh = (r & 1) * 16;
+        pb[n][0][0] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(p00))) << sh;
+        pb[n][0][1] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(p01))) << sh;
+        pb[n][1][0] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(p10))) << sh;
+        pb[n][1][1] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(p11))) << sh;
+      } else {
+        // P^T operand: transpose the fp16 pairs (head 2c, 2c+1) of each 8-token block
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          pb[n][0][t] = movmatrix_trans(pack_half2(__float2half_rn(s[n][0][t]), __float2half_rn(s[n][NGL - 1][t])));
+      }
+    }
+  };
+
+  int n = 0;  // stages consumed (same sequence as the producers')
+  for (int k = 0; k < n_units; ++k) {
+    const UnitStages u = unit_stages<kStageTok>(p, k, ulen_c[k]);
+    consumer_sync<NW>();  // previous unit's merge buffers and q~ are free
+    if (warp < G) {       // q~ = q diag(lambda) H_D * scale * log2(e)
+      const __half2 lo = *reinterpret_cast<const __half2*>(&q_r.x);
+      const __half2 hi = *reinterpret_cast<const __half2*>(&q_r.y);
+      float x[4] = {__low2float(lo) * lam_r.x, __high2float(lo) * lam_r.y,
+                    __low2float(hi) * lam_r.z, __high2float(hi) * lam_r.w};
+      fwht128_warp(x, lane);
+      reinterpret_cast<float4*>(qt + warp * kHeadDim)[lane] =
+          make_float4(x[0] * p.qscale, x[1] * p.qscale, x[2] * p.qscale, x[3] * p.qscale);
+      load_q(k + 1);  // prefetch the next unit's query
+    }
+    consumer_sync<NW>();
+    // B operands of the score mma: k-step kk, rows {2c, 2c+1, 2c+8, 2c+9} hold
+    // dims 32c + 4kk + {0, 1, 2, 3}; column = r.
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const int g = NG == 4 ? (r >> 1) : r;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (g < G) v = reinterpret_cast<const float4*>(qt + g * kHeadDim)[8 * c + kk];
+      uint32_t h01, l01, h23, l23;
+      split_half2(v.x, v.y, h01, l01);
+      split_half2(v.z, v.w, h23, l23);
+      if constexpr (NG == 4) {
+        const bool lo_col = (r & 1) != 0;
+        qa[kk][0] = lo_col ? l01 : h01;
+        qa[kk][1] = lo_col ? l23 : h23;
+      } else {
+        qa[kk][0] = h01;
+        qa[kk][1] = h23;
+        qb[kk][0] = l01;
+        qb[kk][1] = l23;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) O[i][jj] = 0.f;
+#pragma unroll
+    for (int gi = 0; gi < NGL; ++gi) {
+      m_run[gi] = -INFINITY;
+      l_run[gi] = 0.f;
+    }
+#pragma unroll
+    for (int nn = 0; nn < kNCH; ++nn) {  // nothing pending yet
+      pb[nn][0][0] = pb[nn][0][1] = pb[nn][1][0] = pb[nn][1][1] = 0u;
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) pvc[nn][jj] = VCodes<DV, BV>{};
+    }
+
+    for (int j = 0; j < u.count; ++j, ++n) {
+      const int slot = n & (NS - 1);
+      bool ok = !*abort_flag &&
+                mbar_wait_bounded(full + slot, static_cast<uint32_t>(n >> ns_shift) & 1u, abort_flag,
+                                  p.timeout_ns);
+      ok = __all_sync(kFull, ok);
+      if (!ok && lane == 0 && !*abort_flag) {
+        *abort_flag = 1;
+        report(p.status, kDevTimeout);
+      }
+      const int4 m = meta[slot];
+      const int off = warp * kSlice;             // slice offset inside the stage
+      const int tok0 = m.x + off;                // first token of the slice
+      const uint32_t bits = (static_cast<uint32_t>(m.z) >> (kNCH * warp)) & ((1u << kNCH) - 1u);
+      load_codes(stages + static_cast<size_t>(slot) * stage_bytes, off);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + slot);  // codes are in registers: the slot may be refilled
+      float sc[kNCH][4];
+      fused(sc, true);                           // scores now, P.V of the previous stage
+      // tokens past the end, and chunks whose page was invalid, get p = 0
+      softmax(sc, tok0, m.y, (ok && tok0 < m.y) ? bits : 0u);
+#pragma unroll
+      for (int nn = 0; nn < kNCH; ++nn)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) pvc[nn][jj] = vc[nn][jj];
+    }
+    {  // P.V of the unit's last stage
+      float sc[kNCH][4];
+      fused(sc, false);
+    }
+
+    // ---- merge the consumer warps of this unit, write the split partial ------
+#pragma unroll
+    for (int gi = 0; gi < NGL; ++gi) {
+      l_run[gi] += __shfl_xor_sync(kFull, l_run[gi], 4);
+      l_run[gi] += __shfl_xor_sync(kFull, l_run[gi], 8);
+      l_run[gi] += __shfl_xor_sync(kFull, l_run[gi], 16);
+    }
+    if constexpr (NG == 4) {
+      if (c < G) {
+        float4* mo = reinterpret_cast<float4*>(merge + (warp * G + c) * kHeadDim + 16 * r);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mo[i] = make_float4(O[i][0], O[i][1], O[i][2], O[i][3]);
+        if (r == 0) mlbuf[warp * G + c] = make_float2(m_run[0], l_run[0]);
+      }
+    } else {
+#pragma unroll
+      for (int gi = 0; gi < NGL; ++gi) {
+        const int g = 2 * c + gi;
+        if (g < G) {
+          float4* mo = reinterpret_cast<float4*>(merge + (warp * G + g) * kHeadDim + 16 * r);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            mo[i] = make_float4(O[2 * i][gi], O[2 * i][2 + gi], O[2 * i + 1][gi], O[2 * i + 1][2 + gi]);
+          if (r == 0) mlbuf[warp * G + g] = make_float2(m_run[gi], l_run[gi]);
+        }
+      }
+    }
+    consumer_sync<NW>();
+    for (int i = tid; i < G * kHeadDim; i += kConsumerThreads) {
+      const int g = i / kHeadDim, d = i % kHeadDim;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, mlbuf[w * G + g].x);
+      float o = 0.f, l = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float2 ml = mlbuf[w * G + g];
+          const float f = fast_exp2(ml.x - M);
+          o = fmaf(f, merge[(w * G + g) * kHeadDim + d], o);
+          l = fmaf(f, ml.y, l);
+        }
+      }
+      const long long row = (static_cast<long long>(u.b) * p.hq + u.kvh * G + g) * p.splits + u.s;
+      p.ws_o[row * kHeadDim + d] = o;
+      if (d == 0) p.ws_ml[row] = make_float2(M, l);
+    }
+  }
+  __syncthreads();  // matches the producers' final barrier
+}
+
+// Merge of the split partials: o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
+__global__ void __launch_bounds__(kHeadDim) vq_combine_kernel(const CombineParams p) {
+  extern __shared__ float2 cml[];  // [splits]
+  const int row = blockIdx.x, d = threadIdx.x;
+  const float2* ml = p.ws_ml + static_cast<long long>(row) * p.splits;
+  const float* o = p.ws_o + static_cast<long long>(row) * p.splits * kHeadDim + d;
+  for (int s = d; s < p.splits; s += kHeadDim) cml[s] = ml[s];
+  __syncthreads();
+  float M = -INFINITY;
+  for (int s = 0; s < p.splits; ++s) M = fmaxf(M, cml[s].x);
+  float acc = 0.f, l = 0.f;
+  if (M != -INFINITY) {
+#pragma unroll 16
+    for (int s = 0; s < p.splits; ++s) {
+      const float2 v = cml[s];
+      const float f = fast_exp2(v.x - M);
+      acc = fmaf(f, __ldg(o + s * kHeadDim), acc);
+      l = fmaf(f, v.y, l);
+    }
+  }
+  const float res = l > 0.f ? acc / l : 0.f;
+  static_cast<__half*>(p.out)[static_cast<long long>(row) * kHeadDim + d] = __float2half_rn(res);
+}
+
+template <typename K>
+cudaError_t configure(K kern, size_t smem) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
+}
+
+template <int DK, int BK, int DV, int BV, int NG, int NW, int NCH>
+cudaError_t launch_split(const DecodeParams& p, int grid, size_t smem, cudaStream_t stream) {
+  auto kern = vq_decode_split_kernel<DK, BK, DV, BV, NG, NW, NCH>;
+  static size_t configured = 0;
+  if (smem > configured) {
+    cudaError_t e = configure(kern, smem);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  kern<<<grid, (NW + kProducerWarps) * 32, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int DK, int BK, int DV, int BV>
+cudaError_t launch_formats(const DecodeParams& p, int grid, size_t smem, cudaStream_t stream) {
+  const bool wide = p.group > 4;
+  if (p.warps == 12 && p.chunks == 1)
+    return wide ? launch_split<DK, BK, DV, BV, 8, 12, 1>(p, grid, smem, stream)
+                : launch_split<DK, BK, DV, BV, 4, 12, 1>(p, grid, smem, stream);
+  if (p.warps == 8 && p.chunks == 2)
+    return wide ? launch_split<DK, BK, DV, BV, 8, 8, 2>(p, grid, smem, stream)
+                : launch_split<DK, BK, DV, BV, 4, 8, 2>(p, grid, smem, stream);
+  if (p.warps == 8 && p.chunks == 1)
+    return wide ? launch_split<DK, BK, DV, BV, 8, 8, 1>(p, grid, smem, stream)
+                : launch_split<DK, BK, DV, BV, 4, 8, 1>(p, grid, smem, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams& p, int k_sub, int k_bits, int v_sub, int v_bits,
+                          int grid, size_t smem, cudaStream_t stream) {
+#define VQ_CASE(DK, BK, DV, BV) \
+  if (k_sub == DK && k_bits == BK && v_sub == DV && v_bits == BV) return launch_formats<DK, BK, DV, BV>(p, grid, smem, stream);
+  VQ_CASE(2, 8, 4, 8)
+  VQ_CASE(4, 8, 4, 8)
+  VQ_CASE(2, 8, 4, 9)
+  VQ_CASE(4, 8, 4, 9)
+  VQ_CASE(2, 8, 2, 8)
+  VQ_CASE(4, 8, 2, 8)
+#undef VQ_CASE
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
+  if (p.rows == 0) return cudaSuccess;
+  static bool configured = false;
+  const size_t smem = static_cast<size_t>(p.splits) * sizeof(float2);
+  if (!configured) {
+    cudaError_t e = configure(vq_combine_kernel, 48 * 1024);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  vq_combine_kernel<<<p.rows, kHeadDim, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace vqk

@@ -1,0 +1,292 @@
+// vq_encode.cu -- K/V encode kernel (cache fill) for sm_103a.
+//
+// VecInfer, section 方法细节: keys are smoothed and Hadamard transformed,
+// k~ = k diag(lambda)^-1 H_D ("异常值抑制的向量量化"), then keys and raw values are
+// vector-quantized with the offline codebooks and the indices appended to the
+// cache ("注意力机制中的向量量化KV缓存").  Nearest centroid as in section
+// 背景知识 "向量量化原理": j* = argmin_j ||x_i - C_j||^2 per sub-vector.
+//
+// One warp owns one token-head vector (128 fp16 values, 4 per lane).  The key
+// transform runs in fp32 registers: divide by lambda, 7 butterfly stages
+// (2 in registers, 5 by shuffle), scale by 1/sqrt(128).  Each lane then owns
+// the sub-vectors covering its 4 elements and scans the codebook, which the
+// CTA keeps in shared memory as (-2 c_j, ||c_j||^2) in fp32: the score
+// ||c_j||^2 - 2 x.c_j orders centroids exactly as ||x - c_j||^2 does.  All
+// lanes read the same centroid at once (a shared-memory broadcast), so the
+// scan is bound by the FP32 pipe.  With few tokens (a decode-step append) the
+// scan of one vector is split over `split` warps that each take a slice of the
+// codebook, and the slices are merged keeping the lowest index on ties.
+// Finally the warp packs the codes into the LSB-first bit stream of the row
+// (one 32-bit word per lane) and stores it into the token's paged slot.
+#include "vq_device.cuh"
+#include "vq_kernels.h"
+
+namespace vqk {
+namespace {
+
+constexpr int kEncWarps = 8;
+
+template <int D>
+struct Scan {
+  static constexpr int kSub = D <= 4 ? 4 / D : 1;  // sub-vectors per lane
+};
+
+// Scans centroids [j0, j1) for the lane's sub-vectors; strict '<' keeps the
+// lowest index among equal scores.
+template <int D>
+__device__ __forceinline__ void scan_centroids(const float (&x)[4], const float* cmul,
+                                               const float* cnorm, int j0, int j1, int lane,
+                                               float (&best)[4], int (&idx)[4]) {
+  constexpr int NS = Scan<D>::kSub;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    best[s] = INFINITY;
+    idx[s] = 0x7fffffff;
+  }
+  if constexpr (D == 8) {
+    const int half = (lane & 1) * 4;
+    for (int j = j0; j < j1; ++j) {
+      const float4 c = *reinterpret_cast<const float4*>(cmul + j * 8 + half);
+      float part = x[0] * c.x;
+      part = fmaf(x[1], c.y, part);
+      part = fmaf(x[2], c.z, part);
+      part = fmaf(x[3], c.w, part);
+      const float other = __shfl_xor_sync(0xffffffffu, part, 1);
+      const float s = cnorm[j] + (part + other);
+      if (s < best[0]) {
+        best[0] = s;
+        idx[0] = j;
+      }
+    }
+  } else if constexpr (D == 4) {
+    for (int j = j0; j < j1; ++j) {
+      const float4 c = *reinterpret_cast<const float4*>(cmul + j * 4);
+      float s = cnorm[j];
+      s = fmaf(x[0], c.x, s);
+      s = fmaf(x[1], c.y, s);
+      s = fmaf(x[2], c.z, s);
+      s = fmaf(x[3], c.w, s);
+      if (s < best[0]) {
+        best[0] = s;
+        idx[0] = j;
+      }
+    }
+  } else if constexpr (D == 2) {
+    for (int j = j0; j < j1; ++j) {
+      const float2 c = *reinterpret_cast<const float2*>(cmul + j * 2);
+      const float n = cnorm[j];
+      const float s0 = fmaf(x[1], c.y, fmaf(x[0], c.x, n));
+      const float s1 = fmaf(x[3], c.y, fmaf(x[2], c.x, n));
+      if (s0 < best[0]) {
+        best[0] = s0;
+        idx[0] = j;
+      }
+      if (s1 < best[1]) {
+        best[1] = s1;
+        idx[1] = j;
+      }
+    }
+  } else {  // D == 1
+    for (int j = j0; j < j1; ++j) {
+      const float c = cmul[j];
+      const float n = cnorm[j];
+#pragma unroll
+      for (int s = 0; s < NS; ++s) {
+        const float v = fmaf(x[s], c, n);
+        if (v < best[s]) {
+          best[s] = v;
+          idx[s] = j;
+        }
+      }
+    }
+  }
+}
+
+// One warp's vector: its location and the values loaded before the codebook
+// barrier, so that every global load of the CTA is in flight at once.
+struct VecIn {
+  bool active;
+  long long t;
+  int h;
+  uint2 raw;        // 4 fp16 elements of the lane
+  float4 lam;       // smoothing factors of those elements (keys)
+  long long slot;
+};
+
+__device__ __forceinline__ VecIn load_vector(const EncodeParams& p, int which) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int group = warp / p.split;
+  const long long th = static_cast<long long>(blockIdx.x) * (kEncWarps / p.split) + group;
+  VecIn in;
+  in.active = th < static_cast<long long>(p.num_tokens) * p.hkv;
+  in.t = in.active ? th / p.hkv : 0;
+  in.h = in.active ? static_cast<int>(th % p.hkv) : 0;
+  in.raw = make_uint2(0, 0);
+  in.lam = make_float4(1.f, 1.f, 1.f, 1.f);
+  in.slot = -1;
+  if (in.active) {
+    in.raw = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.src[which]) +
+                                                  (in.t * p.hkv + in.h) * kHeadDim) +
+                   lane);
+    if (which == 0) in.lam = __ldg(reinterpret_cast<const float4*>(p.lambda + in.h * kHeadDim) + lane);
+    in.slot = __ldg(p.slots + in.t);
+  }
+  return in;
+}
+
+template <int D>
+__device__ void encode_vector(const EncodeParams& p, int which, const VecIn& in, const float* cmul,
+                              const float* cnorm, float* red_best, int* red_idx) {
+  constexpr int NS = Scan<D>::kSub;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = p.split;
+  const int wing = warp % split;
+  const bool active = in.active;
+  const int h = in.h;
+  const int bits = p.bits[which];
+  const int ncent = 1 << bits;
+
+  float x[4];
+  {
+    const __half2 lo = *reinterpret_cast<const __half2*>(&in.raw.x);
+    const __half2 hi = *reinterpret_cast<const __half2*>(&in.raw.y);
+    x[0] = __low2float(lo);
+    x[1] = __high2float(lo);
+    x[2] = __low2float(hi);
+    x[3] = __high2float(hi);
+  }
+  if (which == 0) {  // keys: smoothing then Walsh-Hadamard
+    x[0] = x[0] / in.lam.x;
+    x[1] = x[1] / in.lam.y;
+    x[2] = x[2] / in.lam.z;
+    x[3] = x[3] / in.lam.w;
+    fwht128_warp(x, lane);
+    const float r = 0.08838834764831845f;  // 1/sqrt(128)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[e] *= r;
+  }
+
+  const int j0 = static_cast<int>((static_cast<long long>(wing) * ncent) / split);
+  const int j1 = static_cast<int>((static_cast<long long>(wing + 1) * ncent) / split);
+  float best[4];
+  int idx[4];
+  scan_centroids<D>(x, cmul, cnorm, j0, j1, lane, best, idx);
+
+  if (split > 1) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      red_best[(warp * 32 + lane) * 4 + s] = best[s];
+      red_idx[(warp * 32 + lane) * 4 + s] = idx[s];
+    }
+    __syncthreads();
+    if (wing == 0) {
+      for (int w = 1; w < split; ++w)
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          const float b2 = red_best[((warp + w) * 32 + lane) * 4 + s];
+          if (b2 < best[s]) {  // later slices hold higher indices: strict '<'
+            best[s] = b2;
+            idx[s] = red_idx[((warp + w) * 32 + lane) * 4 + s];
+          }
+        }
+    }
+  }
+  if (wing != 0) return;
+
+  // Pack: lane w assembles 32-bit word w of the row from the codes that overlap
+  // bits [32w, 32w + 32) of the LSB-first stream.
+  const int S = kHeadDim / D;
+  const int row_words = p.row_bytes[which] / 4;
+  const int i_lo = (32 * lane) / bits;
+  const int kmax = 32 / bits + 2;
+  uint32_t word = 0;
+  for (int k = 0; k < kmax; ++k) {
+    const int i = i_lo + k;
+    int own, reg;
+    if constexpr (D == 8) {
+      own = 2 * i;
+      reg = 0;
+    } else {
+      own = i / NS;
+      reg = i % NS;
+    }
+    own = own > 31 ? 31 : own;
+    uint32_t v = 0;
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+      const uint32_t tv = __shfl_sync(0xffffffffu, static_cast<uint32_t>(idx[s]), own);
+      if (s == reg) v = tv;
+    }
+    if (i < S) {
+      const int pos = i * bits - 32 * lane;
+      if (pos < 32 && pos > -bits)
+        word |= static_cast<uint32_t>((static_cast<uint64_t>(v) << (pos + 32)) >> 32);
+    }
+  }
+  if (!active || lane >= row_words) return;
+  const long long slot = in.slot;
+  if (slot < 0) return;  // padding token
+  if (slot >= p.num_slots) {
+    if (lane == 0) report(p.status, kDevBadSlot);
+    return;
+  }
+  const long long page = slot / p.page_size, off = slot % p.page_size;
+  uint8_t* row = p.pool[which] +
+                 ((page * p.hkv + h) * p.page_size + off) * static_cast<long long>(p.row_bytes[which]);
+  reinterpret_cast<uint32_t*>(row)[lane] = word;
+}
+
+__global__ void __launch_bounds__(kEncWarps * 32) vq_encode_kernel(const EncodeParams p) {
+  extern __shared__ __align__(16) float enc_smem[];
+  const int which = blockIdx.y + p.which_base;
+  const int d = p.sub[which];
+  const int ncent = 1 << p.bits[which];
+  float* cmul = enc_smem;                 // [ncent][d]: -2 c_j
+  float* cnorm = cmul + ncent * d;        // [ncent]: ||c_j||^2
+  float* red_best = cnorm + ((ncent + 3) & ~3);
+  int* red_idx = reinterpret_cast<int*>(red_best + kEncWarps * 32 * 4);
+  const VecIn in = load_vector(p, which);
+  const __half* cb = static_cast<const __half*>(p.cb[which]);
+  for (int j = threadIdx.x; j < ncent; j += blockDim.x) {
+    float n = 0.f;
+    for (int e = 0; e < d; ++e) {
+      const float c = __half2float(cb[j * d + e]);
+      cmul[j * d + e] = -2.f * c;
+      n = fmaf(c, c, n);
+    }
+    cnorm[j] = n;
+  }
+  __syncthreads();
+  switch (d) {
+    case 1: encode_vector<1>(p, which, in, cmul, cnorm, red_best, red_idx); break;
+    case 2: encode_vector<2>(p, which, in, cmul, cnorm, red_best, red_idx); break;
+    case 4: encode_vector<4>(p, which, in, cmul, cnorm, red_best, red_idx); break;
+    default: encode_vector<8>(p, which, in, cmul, cnorm, red_best, red_idx); break;
+  }
+}
+
+}  // namespace
+
+size_t encode_smem_bytes(int sub, int bits) {
+  const size_t ncent = size_t(1) << bits;
+  return (ncent * sub + ((ncent + 3) & ~size_t(3))) * 4 + size_t(kEncWarps) * 32 * 4 * 8;
+}
+
+cudaError_t launch_encode(const EncodeParams& p, int grid_x, int grid_y, size_t smem,
+                          cudaStream_t stream) {
+  static size_t configured = 0;
+  if (smem > configured) {
+    cudaError_t e = cudaFuncSetAttribute(vq_encode_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(vq_encode_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  vq_encode_kernel<<<dim3(grid_x, grid_y), kEncWarps * 32, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace vqk

@@ -1,0 +1,106 @@
+// vq_kernels.h -- host-visible parameter blocks and launch entry points of the
+// sm_103a kernels (internal to the library; the public ABI is include/vqattn.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace vqk {
+
+struct EncodeParams {
+  const void* src[2];    // fp16 [T][Hkv][128]: 0 = keys, 1 = values
+  const void* cb[2];     // fp16 codebooks [2^bits][sub]
+  uint8_t* pool[2];      // [num_pages][Hkv][P][row_bytes]
+  int sub[2];
+  int bits[2];
+  int row_bytes[2];
+  const float* lambda;   // fp32 [Hkv][128]
+  const int64_t* slots;  // [T]
+  int32_t* status;
+  long long num_slots;   // num_pages * P
+  int num_tokens;
+  int hkv;
+  int page_size;
+  int split;             // warps per token-head: 1, 2, 4 or 8
+  int which_base;        // blockIdx.y + which_base selects keys (0) or values (1)
+};
+
+struct DecodeParams {
+  const void* q;              // fp16 [B][Hq][128]
+  const float* lambda;        // fp32 [Hkv][128]
+  const void* cb_k;           // fp16 [2^bk][dk]
+  const void* cb_v;           // fp16 [2^bv][dv]
+  const uint8_t* k_pool;
+  const uint8_t* v_pool;
+  const int32_t* page_table;  // [B][max_pages]
+  const int32_t* seq_lens;    // [B]
+  float* ws_o;                // [B][Hq][S][128] unnormalised split outputs
+  float2* ws_ml;              // [B][Hq][S] (running max in log2 units, row sum)
+  int32_t* status;
+  long long num_pages;
+  unsigned long long timeout_ns;
+  int batch, hq, hkv, group;
+  int page_size, max_pages, max_seq_len;
+  int splits, num_units;
+  int k_row, v_row;
+  int nstage;
+  int warps, chunks;          // consumer shape (DecodeShape)
+  float qscale;               // softmax scale * log2(e) / sqrt(128)
+};
+
+struct CombineParams {
+  const float* ws_o;
+  const float2* ws_ml;
+  void* out;                  // fp16 [B][Hq][128]
+  int rows;                   // B * Hq
+  int splits;
+};
+
+constexpr int kProducerWarps = 4;  // TMA-issuing warps (one in four stages each)
+constexpr int kMaxUnitsPerCta = 256;
+constexpr int kUnitTok = 32;       // split boundaries are multiples of this many tokens
+
+// Consumer shape: `warps` consumer warps, each taking `chunks` 16-token mma
+// chunks of every pipeline stage (a stage holds warps * chunks * 16 tokens).
+struct DecodeShape {
+  int warps, chunks;
+  __host__ __device__ int stage_tok() const { return warps * chunks * 16; }
+};
+
+// Shared-memory carve-up of the split attention kernel (bytes, 128-aligned);
+// `warps` is the number of consumer warps.
+struct DecodeSmem {
+  int cbk, cbv, qt, merge, ml, units, meta, bar, flag, stage, total;
+};
+
+__host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
+
+__host__ __device__ inline DecodeSmem decode_smem(int k_bits, int v_bits, int group, int k_row,
+                                                  int v_row, int nstage, int warps, int stage_tok) {
+  DecodeSmem s;
+  int o = 0;
+  s.cbk = o; o = align128(o + (1 << k_bits) * 128);
+  s.cbv = o; o = align128(o + (1 << v_bits) * 128);
+  s.qt = o; o = align128(o + group * 128 * 4);
+  s.merge = o; o = align128(o + warps * group * 128 * 4);
+  s.ml = o; o = align128(o + warps * group * 8);
+  s.units = o; o = align128(o + 2 * kMaxUnitsPerCta * 4);  // consumer and producer copies
+  s.meta = o; o = align128(o + nstage * 16);
+  s.bar = o; o = align128(o + nstage * 2 * 8);
+  s.flag = o; o = align128(o + 16);
+  s.stage = o; o = align128(o + nstage * stage_tok * (k_row + v_row));
+  s.total = o;
+  return s;
+}
+
+// Launchers (return the cudaError_t of the launch).
+cudaError_t launch_encode(const EncodeParams& p, int grid_x, int grid_y, size_t smem,
+                          cudaStream_t stream);
+size_t encode_smem_bytes(int sub, int bits);
+
+// Returns cudaErrorInvalidValue when no kernel is compiled for the formats.
+cudaError_t launch_decode(const DecodeParams& p, int k_sub, int k_bits, int v_sub, int v_bits,
+                          int grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+
+}  // namespace vqk

@@ -1,0 +1,217 @@
+/*
+ * vqattn.h -- C ABI of the GB300 (sm_103a) VQ KV-cache decode-attention library.
+ *
+ * The method is VecInfer's ("VecInfer: Efficient LLM Inference With Low-Bit KV
+ * Cache via Outlier-Suppressed Vector Quantization", papercache.org summary):
+ *   - keys are smoothed per channel and Walsh-Hadamard transformed,
+ *     K~ = K diag(lambda)^-1 H_D  (section 方法细节, "异常值抑制的向量量化");
+ *   - transformed keys and raw values are vector-quantized: every d-long
+ *     sub-vector is replaced by the b-bit index of its nearest codebook
+ *     centroid (section 背景知识, "向量量化原理");
+ *   - a decode query is transformed to q~ = q diag(lambda) H_D and attends
+ *     directly over the codes:  s = q~ VQ^-1(K~_q)^T * scale, p = softmax(s),
+ *     o = p VQ^-1(V_q)  (section 方法细节, "注意力机制中的向量量化KV缓存").
+ *
+ * Conventions shared by every call:
+ *   - All tensor arguments are DEVICE pointers to caller-owned memory unless a
+ *     parameter says "host".  The library never allocates or frees memory.
+ *   - Every call is asynchronous and ordered on the CUDA stream `stream`
+ *     (a cudaStream_t passed as void*; NULL = the legacy default stream).
+ *     No call synchronises the device.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     failed check returns a negative vq_status and launches nothing.
+ *     vq_last_error() then describes the failure (thread-local string).
+ *   - Device-detected failures (an out-of-range page or slot index, a
+ *     pipeline wait that timed out) never fault the GPU: the kernel skips the
+ *     access and stores a nonzero vq_device_status code into `*status` (first
+ *     error wins) when `status` is non-NULL.  The caller zeroes the word and
+ *     reads it after synchronising.
+ *   - fp16 means IEEE binary16, fp32 IEEE binary32, all little-endian, rows
+ *     contiguous (C order).  Device buffers must be 16-byte aligned.
+ *
+ * Cache layout ("pool"): one pool for K codes and one for V codes, each
+ *   [num_pages][num_kv_heads][page_size][row_bytes]  bytes,
+ * where row_bytes = vq_code_row_bytes(head_dim, sub, bits).  Token t of a
+ * sequence lives in logical page t / page_size at offset t % page_size; the
+ * page table maps logical pages to physical pages.  A row holds the
+ * head_dim / sub codes of one token-head as a bit stream: code i occupies bits
+ * [i*bits, (i+1)*bits), least significant bit first (bit m of the stream is bit
+ * m % 8 of byte m / 8); trailing bits are zero.
+ */
+#ifndef VQATTN_H
+#define VQATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum vq_status {
+  VQ_OK = 0,
+  VQ_ERR_INVALID_ARG = -1,   /* null pointer, bad shape, misaligned buffer ... */
+  VQ_ERR_UNSUPPORTED = -2,   /* valid but not implemented (e.g. head_dim != 128) */
+  VQ_ERR_WORKSPACE = -3,     /* workspace smaller than vq_decode_workspace_bytes() */
+  VQ_ERR_CUDA = -4           /* a CUDA runtime call or launch failed */
+} vq_status;
+
+/* Codes a kernel stores into the optional device status word. */
+typedef enum vq_device_status {
+  VQ_DEV_OK = 0,
+  VQ_DEV_BAD_PAGE = 1,       /* page_table entry outside [0, num_pages): page skipped */
+  VQ_DEV_BAD_SLOT = 2,       /* slot_mapping entry >= num_pages * page_size: token skipped */
+  VQ_DEV_TIMEOUT = 3         /* an asynchronous-copy wait exceeded its time limit */
+} vq_device_status;
+
+/*
+ * Shape of one attention layer's quantized KV cache (host struct, read during
+ * the call only).
+ *   head_dim      D; a power of two.  This build implements D = 128.
+ *   num_q_heads   Hq; query head h reads KV head h / (Hq / Hkv).
+ *   num_kv_heads  Hkv; Hq % Hkv == 0 and Hq / Hkv <= 8.
+ *   k_sub,k_bits  d_k, b_k: K sub-vector length and bits per code (2^b_k
+ *                 centroids).  d_k divides D.
+ *   v_sub,v_bits  d_v, b_v: the same for V.
+ *   page_size     tokens per page, a multiple of 16.
+ */
+typedef struct vq_layout {
+  int32_t head_dim;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t k_sub;
+  int32_t k_bits;
+  int32_t v_sub;
+  int32_t v_bits;
+  int32_t page_size;
+} vq_layout;
+
+/*
+ * Bytes of one packed code row: ceil((head_dim / sub) * bits / 8) rounded up
+ * to a multiple of 4.  Index storage follows VecInfer, section 背景知识,
+ * "向量量化原理": (d_h / d) * (b / 8) bytes of indices per vector.
+ * Returns 0 for an invalid combination.
+ */
+size_t vq_code_row_bytes(int32_t head_dim, int32_t sub, int32_t bits);
+
+/*
+ * Checks a layout against what this build implements.  VQ_OK, or
+ * VQ_ERR_INVALID_ARG / VQ_ERR_UNSUPPORTED with vq_last_error() set.
+ * Encode supports sub in {1, 2, 4, 8} and bits in 1..12; decode attention
+ * supports (k_sub, k_bits) in {(2, 8), (4, 8)} and (v_sub, v_bits) in
+ * {(2, 8), (4, 8), (4, 9)}.
+ */
+vq_status vq_check_layout(const vq_layout* layout, int32_t for_decode);
+
+/*
+ * Encode K/V tokens into the code pools (the cache fill of VecInfer, section
+ * 方法细节 "注意力机制中的向量量化KV缓存": prefill encodes every token, decode
+ * encodes each new token and appends its codes).
+ *   For each token t and KV head h:
+ *     k~ = (k[t][h] / lambda[h]) H_D      (fp32 arithmetic, fast WHT)
+ *     K code i = argmin_j ||k~_i - C_k[j]||^2, V code i likewise on raw v
+ *     (lowest index on an exact tie), packed into row
+ *     pool[slot / P][h][slot % P] with slot = slot_mapping[t].
+ *   k, v          fp16 [num_tokens][Hkv][D].  Either may be NULL (that half is
+ *                 not encoded), not both.
+ *   slot_mapping  int64 [num_tokens].  A negative slot skips the token; a slot
+ *                 >= num_pages * P skips it and reports VQ_DEV_BAD_SLOT.
+ *   lambda        fp32 [Hkv][D] smoothing factors (lambda, not 1/lambda),
+ *                 all > 0.  Required when k is non-NULL.
+ *   codebook_k    fp16 [2^k_bits][k_sub]; codebook_v fp16 [2^v_bits][v_sub].
+ *   k_pool,v_pool pools as described above, num_pages pages each.
+ *   status        optional device int32 status word.
+ * num_tokens == 0 is a no-op returning VQ_OK.
+ */
+vq_status vq_encode_kv(const vq_layout* layout, int32_t num_tokens,
+                       const void* k, const void* v, const int64_t* slot_mapping,
+                       const float* lambda, const void* codebook_k, const void* codebook_v,
+                       void* k_pool, void* v_pool, int64_t num_pages,
+                       int32_t* status, void* stream);
+
+/*
+ * Workspace bytes vq_decode_attention needs for `batch` sequences split
+ * `num_splits` ways (num_splits <= 0: the value vq_default_num_splits picks).
+ * Pure host arithmetic.  Returns 0 for invalid arguments.
+ */
+size_t vq_decode_workspace_bytes(const vq_layout* layout, int32_t batch,
+                                 int32_t max_seq_len, int32_t num_splits, int32_t num_sms);
+
+/*
+ * Split-K factor the library picks for a batch: the number of sequence
+ * splits per (sequence, KV head) that balances work units over num_sms SMs
+ * (num_sms <= 0: query the current device).  Returns >= 1, or 0 on error.
+ */
+int32_t vq_default_num_splits(const vq_layout* layout, int32_t batch, int32_t max_seq_len,
+                              int32_t num_sms);
+
+/*
+ * Decode attention for one query token per sequence over the quantized cache
+ * (VecInfer, section 方法细节 "注意力机制中的向量量化KV缓存"; split-K with an
+ * online-softmax merge as in the FlashAttention recurrence of the appendix
+ * "相关工作 - FlashAttention").
+ *   q            fp16 [batch][Hq][D] decode queries (untransformed).
+ *   lambda       fp32 [Hkv][D] smoothing factors used when the keys were encoded.
+ *   codebook_k/v fp16 codebooks used when the caches were encoded.
+ *   k_pool/v_pool the pools (num_pages pages each).
+ *   page_table   int32 [batch][max_pages_per_seq]: logical -> physical page.
+ *   seq_lens     int32 [batch]: tokens each query attends to (cached plus
+ *                appended); 0 gives a zero output row.
+ *   max_seq_len  host upper bound of seq_lens, used to size the split grid;
+ *                tokens beyond it are ignored.
+ *   softmax_scale multiplies the scores; 0 selects 1/sqrt(D).
+ *   num_splits   sequence splits per (sequence, KV head); <= 0 selects the
+ *                library's choice.  Results do not depend on it beyond
+ *                fp32 rounding.
+ *   out          fp16 [batch][Hq][D] attention output.
+ *   workspace    device scratch of at least vq_decode_workspace_bytes(...)
+ *                bytes (fp32 partial results of the splits); 256-byte aligned.
+ *   status       optional device int32 status word.
+ * Two kernels are launched on `stream`: the split attention kernel and the
+ * split-combine kernel.
+ */
+vq_status vq_decode_attention(const vq_layout* layout, int32_t batch, const void* q,
+                              const float* lambda, const void* codebook_k,
+                              const void* codebook_v, const void* k_pool, const void* v_pool,
+                              int64_t num_pages, const int32_t* page_table,
+                              int32_t max_pages_per_seq, const int32_t* seq_lens,
+                              int32_t max_seq_len, float softmax_scale, int32_t num_splits,
+                              void* out, void* workspace, size_t workspace_bytes,
+                              int32_t* status, void* stream);
+
+/*
+ * The two halves of vq_decode_attention, for callers that schedule them
+ * separately (for example to overlap the combine with other work):
+ *   vq_decode_partial  takes the arguments of vq_decode_attention except `out`
+ *                      and launches only the split attention kernel, which
+ *                      writes one (max, sum, unnormalised output) partial per
+ *                      (sequence, query head, split) into the workspace;
+ *   vq_decode_combine  launches only the merge of those partials into `out`
+ *                      (fp16 [batch][Hq][D]).
+ * Both must be called with the same layout, batch, max_seq_len, num_splits and
+ * workspace, on the same device and stream order; num_splits <= 0 resolves to
+ * the same value in both calls.
+ */
+vq_status vq_decode_partial(const vq_layout* layout, int32_t batch, const void* q,
+                            const float* lambda, const void* codebook_k, const void* codebook_v,
+                            const void* k_pool, const void* v_pool, int64_t num_pages,
+                            const int32_t* page_table, int32_t max_pages_per_seq,
+                            const int32_t* seq_lens, int32_t max_seq_len, float softmax_scale,
+                            int32_t num_splits, void* workspace, size_t workspace_bytes,
+                            int32_t* status, void* stream);
+
+vq_status vq_decode_combine(const vq_layout* layout, int32_t batch, int32_t max_seq_len,
+                            int32_t num_splits, const void* workspace, size_t workspace_bytes,
+                            void* out, void* stream);
+
+/* Human-readable description of the last non-OK status on this host thread. */
+const char* vq_last_error(void);
+
+/* Library version string, e.g. "vqattn 0.1.0 sm_103a". */
+const char* vq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VQATTN_H */

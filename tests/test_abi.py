@@ -1,0 +1,118 @@
+"""The C ABI library: loads, exports every declared symbol, host-side logic.
+
+No test here launches a kernel: every call either is pure host arithmetic or
+fails argument validation before anything reaches the GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_vector_quantized_gb300 as vq
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "vqattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(vq.LIB_PATH):
+        from bit_vector_quantized_gb300 import build
+        build.build()
+    return vq.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vq_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) == set(vq.EXPORTED)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version(lib):
+    assert "sm_103a" in vq.vq_version()
+
+
+@pytest.mark.parametrize("d,sub,bits,expect", [(128, 4, 8, 32), (128, 2, 8, 64), (128, 4, 9, 36),
+                                                (128, 8, 12, 24), (128, 1, 1, 16), (128, 3, 8, 0),
+                                                (128, 4, 0, 0), (0, 4, 8, 0)])
+def test_code_row_bytes(lib, d, sub, bits, expect):
+    assert vq.vq_code_row_bytes(d, sub, bits) == expect
+
+
+def test_check_layout(lib):
+    vq.vq_check_layout(vq.make_layout(), True)
+    vq.vq_check_layout(vq.make_layout(k_sub=2, v_bits=9, num_q_heads=40), True)
+    vq.vq_check_layout(vq.make_layout(k_sub=8, k_bits=12), False)
+    cases = [(dict(head_dim=96), vq.VQ_ERR_INVALID_ARG), (dict(head_dim=64), vq.VQ_ERR_UNSUPPORTED),
+             (dict(num_q_heads=30), vq.VQ_ERR_INVALID_ARG), (dict(num_q_heads=72), vq.VQ_ERR_UNSUPPORTED),
+             (dict(k_sub=3), vq.VQ_ERR_INVALID_ARG), (dict(v_bits=13), vq.VQ_ERR_INVALID_ARG),
+             (dict(page_size=40), vq.VQ_ERR_INVALID_ARG)]
+    for kw, st in cases:
+        with pytest.raises(vq.VQError) as e:
+            vq.vq_check_layout(vq.make_layout(**kw), False)
+        assert e.value.status == st
+    with pytest.raises(vq.VQError) as e:
+        vq.vq_check_layout(vq.make_layout(k_sub=8, k_bits=12), True)
+    assert e.value.status == vq.VQ_ERR_UNSUPPORTED and "decode" in vq.vq_last_error()
+
+
+def test_split_heuristic_and_workspace(lib):
+    L1 = vq.make_layout()
+    assert vq.vq_default_num_splits(L1, 1, 32769, 152) == 19          # 8 heads x 19 = 152 units
+    assert vq.vq_default_num_splits(L1, 1, 196609, 152) == 19
+    L4 = vq.make_layout(num_q_heads=40, k_sub=2, v_bits=9)
+    s4 = vq.vq_default_num_splits(L4, 64, 16385, 152)
+    assert 1 <= s4 <= 8
+    assert vq.vq_default_num_splits(L1, 1, 0, 152) == 1
+    n = vq.vq_decode_workspace_bytes(L1, 1, 32769, 19, 152)
+    assert n >= 32 * 19 * (128 + 2) * 4 and n % 256 == 0
+    assert vq.vq_decode_workspace_bytes(L1, -1, 10, 0, 152) == 0
+
+
+FAKE = 1 << 20  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def test_encode_rejects_bad_arguments(lib):
+    L = vq.make_layout()
+    args = dict(layout=L, num_tokens=4, k=FAKE, v=FAKE, slot_mapping=FAKE, lambda_=FAKE,
+                codebook_k=FAKE, codebook_v=FAKE, k_pool=FAKE, v_pool=FAKE, num_pages=4)
+    bad = [dict(num_tokens=-1), dict(k=None, v=None), dict(slot_mapping=None), dict(num_pages=0),
+           dict(lambda_=None), dict(codebook_v=None), dict(k=FAKE + 4), dict(v_pool=FAKE + 8),
+           dict(layout=vq.make_layout(page_size=8))]
+    for kw in bad:
+        a = dict(args, **kw)
+        with pytest.raises(vq.VQError) as e:
+            vq.vq_encode_kv(**a)
+        assert e.value.status == vq.VQ_ERR_INVALID_ARG, kw
+
+
+def test_decode_rejects_bad_arguments(lib):
+    L = vq.make_layout()
+    args = dict(layout=L, batch=1, q=FAKE, lambda_=FAKE, codebook_k=FAKE, codebook_v=FAKE,
+                k_pool=FAKE, v_pool=FAKE, num_pages=4, page_table=FAKE, max_pages_per_seq=4,
+                seq_lens=FAKE, max_seq_len=100, softmax_scale=0.0, num_splits=0, out=FAKE,
+                workspace=FAKE, workspace_bytes=1 << 30)
+    bad = [(dict(batch=-2), vq.VQ_ERR_INVALID_ARG), (dict(q=None), vq.VQ_ERR_INVALID_ARG),
+           (dict(out=FAKE + 2), vq.VQ_ERR_INVALID_ARG), (dict(max_seq_len=5000), vq.VQ_ERR_INVALID_ARG),
+           (dict(max_pages_per_seq=0), vq.VQ_ERR_INVALID_ARG),
+           (dict(softmax_scale=float("nan")), vq.VQ_ERR_INVALID_ARG),
+           (dict(num_splits=5000), vq.VQ_ERR_INVALID_ARG),
+           (dict(layout=vq.make_layout(v_sub=8)), vq.VQ_ERR_UNSUPPORTED)]
+    for kw, st in bad:
+        with pytest.raises(vq.VQError) as e:
+            vq.vq_decode_attention(**dict(args, **kw))
+        assert e.value.status == st, kw
+
+
+def test_empty_calls_are_noops(lib):
+    L = vq.make_layout()
+    vq.vq_encode_kv(L, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4)
+    vq.vq_decode_attention(L, 0, None, None, None, None, None, None, 1, None, 1, None, 0, 0.0, 0,
+                           None, None, 0)

@@ -1,0 +1,241 @@
+"""Shared harness of the GPU parity tests (not a test module).
+
+Builds one workload's caches on the GPU through the C ABI and the matching
+oracle results on the CPU from the same seeded inputs.  Inputs flow only from
+the generators (and the oracle) to the GPU, never from the GPU to the oracle.
+"""
+from __future__ import annotations
+
+import csv
+import os
+from dataclasses import dataclass
+from typing import Dict, List, Optional, Tuple
+
+import numpy as np
+
+import oracle
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+TIE_REL = 1e-6        # ties: centroid distances within 1e-6 relative (see tie_band)
+MAX_ABS = 2e-3        # attention output tolerance, fp16 inputs / fp32 accumulation
+MEAN_ABS = 2e-4
+
+
+@dataclass
+class Calib:
+    lam: np.ndarray    # fp32 [Hkv][D]
+    ck: np.ndarray     # fp16 [2^bk][dk]
+    cv: np.ndarray     # fp16 [2^bv][dv]
+
+
+def stored_calib(i: int) -> Calib:
+    z = np.load(os.path.join(GOLDEN, "calib", f"cfg{i}.npz"))
+    return Calib(z["lam"], z["ck"], z["cv"])
+
+
+_small_cache: Dict[tuple, Calib] = {}
+
+
+def small_calib(w: W.Workload, n_cal: int = 2048, iters: int = 6) -> Calib:
+    """Oracle calibration on a subsample (tests of shapes without stored files)."""
+    key = (w.num_kv_heads, w.k_sub, w.k_bits, w.v_sub, w.v_bits, w.drift, w.context)
+    if key not in _small_cache:
+        k_cal, v_cal = W.calibration(w)
+        k_cal, v_cal = k_cal[:n_cal], v_cal[:n_cal]
+        lam = oracle.smoothing_lambda(k_cal).astype(np.float32)
+        xk = oracle.transform_keys(k_cal, lam).reshape(-1, w.k_sub)
+        xv = v_cal.astype(np.float64).reshape(-1, w.v_sub)
+        ck, _ = oracle.kmeans(xk, W.kmeans_init(len(xk), 2 ** w.k_bits, "k"), iters)
+        cv, _ = oracle.kmeans(xv, W.kmeans_init(len(xv), 2 ** w.v_bits, "v"), iters)
+        _small_cache[key] = Calib(lam, ck.astype(np.float16), cv.astype(np.float16))
+    return _small_cache[key]
+
+
+def calib_for(w: W.Workload) -> Calib:
+    if 0 <= w.index < len(W.WORKLOADS):
+        return stored_calib(w.index)
+    return small_calib(w)
+
+
+# ------------------------------------------------------------------ oracle ---
+
+@dataclass
+class OracleSeq:
+    kc: np.ndarray          # int32 [T][Hkv][Sk]
+    vc: np.ndarray          # int32 [T][Hkv][Sv]
+    kx: np.ndarray          # fp64 transformed keys [T][Hkv][D]
+    vx: np.ndarray          # fp64 values [T][Hkv][D]
+
+
+def oracle_encode(w: W.Workload, cal: Calib, b: int, start: int = 0,
+                  stop: Optional[int] = None, heads: Optional[List[int]] = None) -> OracleSeq:
+    k = W.kv_tokens(w, b, "k", start, stop)
+    v = W.kv_tokens(w, b, "v", start, stop)
+    lam = cal.lam
+    if heads is not None:
+        k, v, lam = k[:, heads], v[:, heads], lam[heads]
+    kc, kx, _, _ = oracle.encode_keys(k, lam.astype(np.float64), cal.ck, w.k_sub)
+    vc, vx, _, _ = oracle.encode_values(v, cal.cv, w.v_sub)
+    return OracleSeq(kc, vc, kx, vx)
+
+
+def oracle_attention(w: W.Workload, cal: Calib, q_b: np.ndarray, kc, vc,
+                     heads: Optional[List[int]] = None) -> np.ndarray:
+    """fp64 [Hq'][D] over codes (KV heads `heads`, all by default)."""
+    lam = cal.lam if heads is None else cal.lam[heads]
+    return oracle.decode_attention(q_b, lam.astype(np.float64), kc, cal.ck, vc, cal.cv)
+
+
+def tie_band(x: np.ndarray, C: np.ndarray, j_gpu: np.ndarray, j_orc: np.ndarray):
+    """Distance gap and allowed band for code mismatches (rows of sub-vectors x).
+
+    A GPU code j' that differs from the oracle's j* is accepted, and logged, when
+    ||x - C[j']||^2 - ||x - C[j*]||^2 <= 1e-6 * (||x||^2 + max(||C[j']||^2, ||C[j*]||^2)):
+    the scale of the terms an fp32 evaluation of the distance cancels.
+    """
+    Cf = C.astype(np.float64)
+    dg = ((x - Cf[j_gpu]) ** 2).sum(-1)
+    do = ((x - Cf[j_orc]) ** 2).sum(-1)
+    scale = (x ** 2).sum(-1) + np.maximum((Cf[j_gpu] ** 2).sum(-1), (Cf[j_orc] ** 2).sum(-1))
+    return dg - do, TIE_REL * scale
+
+
+def compare_codes(gpu: np.ndarray, orc: np.ndarray, x: np.ndarray, C: np.ndarray, d: int,
+                  label: str, log_rows: list) -> int:
+    """Asserts bit-exact codes except in-band ties; returns the number of ties."""
+    assert gpu.shape == orc.shape, (gpu.shape, orc.shape)
+    mism = np.argwhere(gpu != orc)
+    if len(mism) == 0:
+        return 0
+    xs = x.reshape(x.shape[:-1] + (x.shape[-1] // d, d))
+    sel = tuple(mism.T)
+    gap, band = tie_band(xs[sel], C, gpu[sel], orc[sel])
+    for (idx, g, o, gp, bd) in zip(mism.tolist(), gpu[sel], orc[sel], gap, band):
+        log_rows.append([label, idx, int(g), int(o), float(gp), float(bd)])
+    bad = gap > band
+    assert not bad.any(), (f"{label}: {int(bad.sum())} of {len(mism)} code mismatches are outside "
+                           f"the tie band, e.g. index {mism[np.argmax(bad)].tolist()} gap "
+                           f"{gap[bad][0]:.3e} band {band[bad][0]:.3e}")
+    return len(mism)
+
+
+def write_tie_log(name: str, rows: list) -> Optional[str]:
+    """Tie log as CSV under $VQ_TIE_LOG_DIR (default: gpurun_out if present, else none)."""
+    d = os.environ.get("VQ_TIE_LOG_DIR") or ("gpurun_out" if os.path.isdir("gpurun_out") else None)
+    if not d or not rows:
+        return None
+    os.makedirs(d, exist_ok=True)
+    path = os.path.join(d, f"ties_{name}.csv")
+    with open(path, "w", newline="") as f:
+        wr = csv.writer(f)
+        wr.writerow(["what", "index", "gpu_code", "oracle_code", "dist_gap", "band"])
+        wr.writerows(rows)
+    return path
+
+
+def check_outputs(got: np.ndarray, ref: np.ndarray, label: str) -> Tuple[float, float]:
+    err = np.abs(got.astype(np.float64) - ref)
+    mx, mean = float(err.max()) if err.size else 0.0, float(err.mean()) if err.size else 0.0
+    assert mx <= MAX_ABS and mean <= MEAN_ABS, f"{label}: max-abs {mx:.3e}, mean-abs {mean:.3e}"
+    return mx, mean
+
+
+# --------------------------------------------------------------------- GPU ---
+
+class GpuCache:
+    """One workload's paged code pools on the GPU, filled through vq_encode_kv."""
+
+    def __init__(self, w: W.Workload, cal: Calib, device: str = "cuda"):
+        import torch
+        import bit_vector_quantized_gb300 as vq
+        self.torch, self.vq, self.w, self.cal, self.device = torch, vq, w, cal, device
+        self.layout = vq.make_layout(w.head_dim, w.num_q_heads, w.num_kv_heads, w.k_sub,
+                                     w.k_bits, w.v_sub, w.v_bits, w.page_size)
+        self.lens = W.seq_lens(w)
+        self.num_pages = W.num_pages(w)
+        self.k_pool, self.v_pool = vq.alloc_pools(self.layout, self.num_pages, device, zero=True)
+        self.page_table_np = W.page_table(w)
+        self.page_table = torch.from_numpy(self.page_table_np).to(device)
+        self.lam = torch.from_numpy(cal.lam).to(device)
+        self.ck = torch.from_numpy(cal.ck).to(device)
+        self.cv = torch.from_numpy(cal.cv).to(device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.krow, self.vrow = vq.row_bytes(self.layout)
+
+    def encode(self, b: int, start: int, stop: int, k=None, v=None) -> None:
+        t = self.torch
+        if k is None:
+            k = W.kv_tokens(self.w, b, "k", start, stop)
+        if v is None:
+            v = W.kv_tokens(self.w, b, "v", start, stop)
+        slots = t.from_numpy(W.slot_mapping(self.w, b, start, stop)).to(self.device)
+        self.vq.encode_kv(self.layout, t.from_numpy(np.ascontiguousarray(k)).to(self.device),
+                          t.from_numpy(np.ascontiguousarray(v)).to(self.device), slots,
+                          self.lam, self.ck, self.cv, self.k_pool, self.v_pool, status=self.status)
+
+    def prefill(self, block: int = 65536) -> None:
+        for b in range(self.w.batch):
+            n = int(self.lens[b])
+            for s in range(0, n, block):
+                self.encode(b, s, min(n, s + block))
+
+    def append(self) -> None:
+        """Decode-step append: token N_b of every sequence in one call."""
+        t = self.torch
+        k = np.stack([W.kv_tokens(self.w, b, "k", int(n), int(n) + 1)[0] for b, n in enumerate(self.lens)])
+        v = np.stack([W.kv_tokens(self.w, b, "v", int(n), int(n) + 1)[0] for b, n in enumerate(self.lens)])
+        slots = np.array([W.slot_mapping(self.w, b, int(n), int(n) + 1)[0]
+                          for b, n in enumerate(self.lens)], dtype=np.int64)
+        self.vq.encode_kv(self.layout, t.from_numpy(k).to(self.device), t.from_numpy(v).to(self.device),
+                          t.from_numpy(slots).to(self.device), self.lam, self.ck, self.cv,
+                          self.k_pool, self.v_pool, status=self.status)
+
+    def decode(self, q: Optional[np.ndarray] = None, lens: Optional[np.ndarray] = None,
+               num_splits: int = 0, softmax_scale: float = 0.0) -> np.ndarray:
+        t = self.torch
+        q = W.queries(self.w) if q is None else q
+        lens = self.lens + 1 if lens is None else lens
+        seq = t.from_numpy(lens.astype(np.int32)).to(self.device)
+        out = self.vq.decode_attention(self.layout, t.from_numpy(q).to(self.device), self.lam,
+                                       self.ck, self.cv, self.k_pool, self.v_pool, self.page_table,
+                                       seq, int(lens.max()) if len(lens) else 0,
+                                       num_splits=num_splits, softmax_scale=softmax_scale,
+                                       status=self.status)
+        t.cuda.synchronize()
+        return out.float().cpu().numpy()
+
+    def device_status(self) -> int:
+        self.torch.cuda.synchronize()
+        return int(self.status.item())
+
+    # -- logical views of the pools ---------------------------------------------
+    def _rows(self, pool, b: int, start: int, stop: int, heads=None) -> np.ndarray:
+        t = np.arange(start, stop)
+        pages = self.page_table_np[b][t // self.w.page_size]
+        idx_p = self.torch.from_numpy(pages.astype(np.int64)).to(self.device)
+        idx_o = self.torch.from_numpy((t % self.w.page_size).astype(np.int64)).to(self.device)
+        rows = pool[idx_p, :, idx_o].cpu().numpy()   # [T][Hkv][row]
+        return rows if heads is None else rows[:, heads]
+
+    def codes(self, b: int, start: int, stop: int, heads=None) -> Tuple[np.ndarray, np.ndarray]:
+        kr = self._rows(self.k_pool, b, start, stop, heads)
+        vr = self._rows(self.v_pool, b, start, stop, heads)
+        return (oracle.unpack(kr, 128 // self.w.k_sub, self.w.k_bits),
+                oracle.unpack(vr, 128 // self.w.v_sub, self.w.v_bits))
+
+    def write_codes(self, b: int, start: int, kc: np.ndarray, vc: np.ndarray, heads=None) -> None:
+        """Overwrite pool rows of seq b from `start` with (oracle) codes [T][H'][S]."""
+        T = kc.shape[0]
+        t = np.arange(start, start + T)
+        pages = self.page_table_np[b][t // self.w.page_size].astype(np.int64)
+        offs = (t % self.w.page_size).astype(np.int64)
+        heads = list(range(self.w.num_kv_heads)) if heads is None else heads
+        kp = oracle.pack(kc, self.w.k_bits, self.krow)
+        vp = oracle.pack(vc, self.w.v_bits, self.vrow)
+        tt = self.torch
+        P = tt.from_numpy(pages).to(self.device)
+        O = tt.from_numpy(offs).to(self.device)
+        for j, h in enumerate(heads):
+            self.k_pool[P, h, O] = tt.from_numpy(np.ascontiguousarray(kp[:, j])).to(self.device)
+            self.v_pool[P, h, O] = tt.from_numpy(np.ascontiguousarray(vp[:, j])).to(self.device)
