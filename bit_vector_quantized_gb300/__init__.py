@@ -33,7 +33,8 @@ VQ_DEV_OK, VQ_DEV_BAD_PAGE, VQ_DEV_BAD_SLOT, VQ_DEV_TIMEOUT = 0, 1, 2, 3
 # every symbol include/vqattn.h declares
 EXPORTED = ("vq_code_row_bytes", "vq_check_layout", "vq_encode_kv", "vq_decode_workspace_bytes",
             "vq_default_num_splits", "vq_decode_attention", "vq_decode_partial",
-            "vq_decode_combine", "vq_last_error", "vq_version")
+            "vq_decode_combine", "vq_decode_attention_static", "vq_static_scratch_bytes",
+            "vq_last_error", "vq_version")
 
 
 class VQError(RuntimeError):
@@ -81,6 +82,9 @@ def lib() -> ctypes.CDLL:
             "vq_decode_partial": (I32, [LP, I32, P, P, P, P, P, P, I64, P, I32, P, I32,
                                         ctypes.c_float, I32, P, SZ, P, P]),
             "vq_decode_combine": (I32, [LP, I32, I32, I32, P, SZ, P, P]),
+            "vq_decode_attention_static": (I32, [LP, I32, P, P, P, P, P, P, I64, P, I32, P, I32,
+                                                 ctypes.c_float, I32, P, P, P]),
+            "vq_static_scratch_bytes": (SZ, []),
             "vq_last_error": (ctypes.c_char_p, []),
             "vq_version": (ctypes.c_char_p, []),
         }
@@ -155,6 +159,23 @@ def vq_decode_combine(layout, batch, max_seq_len, num_splits, workspace, workspa
                       stream=None) -> None:
     _check(lib().vq_decode_combine(ctypes.byref(layout), batch, max_seq_len, num_splits,
                                    _ptr(workspace), workspace_bytes, _ptr(out), _ptr(stream)))
+
+
+def vq_decode_attention_static(layout, batch, q, lambda_, codebook_k, codebook_v, k_pool, v_pool,
+                               num_pages, page_table, max_pages_per_seq, seq_lens, max_seq_len,
+                               softmax_scale, num_splits, out, status=None, stream=None) -> None:
+    """vq_decode_attention for callers that cannot allocate: no workspace argument;
+    the split partials live in the library's fixed device array (see the header)."""
+    _check(lib().vq_decode_attention_static(ctypes.byref(layout), batch, _ptr(q), _ptr(lambda_),
+                                            _ptr(codebook_k), _ptr(codebook_v), _ptr(k_pool),
+                                            _ptr(v_pool), num_pages, _ptr(page_table),
+                                            max_pages_per_seq, _ptr(seq_lens), max_seq_len,
+                                            float(softmax_scale), num_splits, _ptr(out),
+                                            _ptr(status), _ptr(stream)))
+
+
+def vq_static_scratch_bytes() -> int:
+    return int(lib().vq_static_scratch_bytes())
 
 
 def vq_last_error() -> str:

@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "../../include/vqattn.h"
@@ -403,6 +404,94 @@ vq_status vq_decode_attention(const vq_layout* layout, int32_t batch, const void
   if (st != VQ_OK) return st;
   return combine_impl(layout, batch, max_seq_len, p.splits, workspace, workspace_bytes, out, stream);
 }
+
+}  // extern "C"
+
+// ---- decode attention without a caller workspace ----------------------------
+// Some callers cannot allocate device memory at the point where they run
+// attention: code that executes inside a region where allocation is forbidden
+// or would synchronise the device, embedders whose memory is owned by a
+// foreign allocator they cannot call, or plug-ins that are handed only the
+// tensors of one call.  For them the split partials live in this fixed,
+// file-scope device array instead of a workspace.  Every GPU that loads the
+// library holds the array until the process exits.
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;  // 4 MiB
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the array on the current device (a host-side name of a
+// __device__ variable is not a device address); looked up once per device.
+vq_status static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(VQ_ERR_UNSUPPORTED, "device %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return VQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+vq_status vq_decode_attention_static(const vq_layout* layout, int32_t batch, const void* q,
+                                     const float* lambda, const void* codebook_k,
+                                     const void* codebook_v, const void* k_pool,
+                                     const void* v_pool, int64_t num_pages,
+                                     const int32_t* page_table, int32_t max_pages_per_seq,
+                                     const int32_t* seq_lens, int32_t max_seq_len,
+                                     float softmax_scale, int32_t num_splits, void* out,
+                                     int32_t* status, void* stream) {
+  vq_status st = check_layout_impl(layout, 1);
+  if (st != VQ_OK) return st;
+  if (batch < 0) return fail(VQ_ERR_INVALID_ARG, "batch %d < 0", batch);
+  if (batch == 0) return VQ_OK;
+  if (!out) return fail(VQ_ERR_INVALID_ARG, "out is NULL");
+  if (!aligned16(out)) return fail(VQ_ERR_INVALID_ARG, "out is not 16-byte aligned");
+  if (max_seq_len < 0) return fail(VQ_ERR_INVALID_ARG, "max_seq_len %d < 0", max_seq_len);
+  if (num_splits > kMaxSplits) return fail(VQ_ERR_INVALID_ARG, "num_splits %d > %d", num_splits, kMaxSplits);
+  int splits = num_splits;
+  if (splits <= 0) {
+    const int sms = device_sms();
+    if (sms <= 0) return fail(VQ_ERR_CUDA, "no CUDA device");
+    splits = pick_splits(*layout, batch, max_seq_len, sms);
+  }
+  const size_t need = ws_layout(*layout, batch, splits).total;
+  if (need > kStaticScratchBytes)
+    return fail(VQ_ERR_WORKSPACE,
+                "batch %d x %d query heads x %d splits needs %zu bytes of split scratch; the static "
+                "scratch holds %zu bytes (use vq_decode_attention with a workspace, or fewer splits)",
+                batch, layout->num_q_heads, splits, need, kStaticScratchBytes);
+  void* scratch = nullptr;
+  st = static_scratch(&scratch);
+  if (st != VQ_OK) return st;
+  // The split kernel writes every partial it later merges, so nothing in the
+  // scratch has to start at zero; stale contents of an earlier call are never read.
+  vqk::DecodeParams p;
+  int grid = 0;
+  size_t smem = 0;
+  st = prepare_decode(layout, batch, q, lambda, codebook_k, codebook_v, k_pool, v_pool, num_pages,
+                      page_table, max_pages_per_seq, seq_lens, max_seq_len, softmax_scale, splits,
+                      scratch, kStaticScratchBytes, status, p, grid, smem);
+  if (st != VQ_OK) return st;
+  st = launch_partial(*layout, p, grid, smem, stream);
+  if (st != VQ_OK) return st;
+  return combine_impl(layout, batch, max_seq_len, splits, scratch, kStaticScratchBytes, out, stream);
+}
+
+size_t vq_static_scratch_bytes(void) { return kStaticScratchBytes; }
 
 const char* vq_last_error(void) { return g_last_error.c_str(); }
 

@@ -204,6 +204,44 @@ vq_status vq_decode_combine(const vq_layout* layout, int32_t batch, int32_t max_
                             int32_t num_splits, const void* workspace, size_t workspace_bytes,
                             void* out, void* stream);
 
+/*
+ * Decode attention for callers that cannot allocate device memory.
+ *
+ * No counterpart on the VecInfer pages: this is a deployment variant of
+ * vq_decode_attention.  Some callers cannot hand the library a workspace:
+ * code running where device allocation is not allowed (or would synchronise
+ * the device), embedders whose memory belongs to an allocator they cannot
+ * call, and plug-ins that receive only the tensors of one call.  This entry
+ * point takes the same arguments as vq_decode_attention minus the workspace
+ * and keeps the split partials in a fixed device array inside the library
+ * instead, so it allocates nothing (no cudaMalloc, no cudaFree, no allocating
+ * library call).
+ *   - The array holds vq_static_scratch_bytes() bytes (4 MiB) on every GPU
+ *     that loads the library, until the process exits.  A request whose
+ *     vq_decode_workspace_bytes() exceeds that returns VQ_ERR_WORKSPACE and
+ *     launches nothing.
+ *   - The first call on a device looks the array's device address up with
+ *     cudaGetSymbolAddress (once per device, for the device that is current);
+ *     make that first call before any stream capture.
+ *   - All calls on a device share the one array, which keeps the contents of
+ *     the last call.  Nothing in it has to start at zero: the split kernel
+ *     writes every partial the combine reads.  Calls whose kernels overlap on
+ *     the GPU (different streams without ordering, or several host threads)
+ *     race on the array and give wrong results; serialise them.
+ * Arguments, validation and outputs are those of vq_decode_attention.
+ */
+vq_status vq_decode_attention_static(const vq_layout* layout, int32_t batch, const void* q,
+                                     const float* lambda, const void* codebook_k,
+                                     const void* codebook_v, const void* k_pool,
+                                     const void* v_pool, int64_t num_pages,
+                                     const int32_t* page_table, int32_t max_pages_per_seq,
+                                     const int32_t* seq_lens, int32_t max_seq_len,
+                                     float softmax_scale, int32_t num_splits, void* out,
+                                     int32_t* status, void* stream);
+
+/* Bytes of the fixed device array vq_decode_attention_static uses. */
+size_t vq_static_scratch_bytes(void);
+
 /* Human-readable description of the last non-OK status on this host thread. */
 const char* vq_last_error(void);
 
