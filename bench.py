@@ -13,9 +13,10 @@ cached tokens (+1 appended), 2-bit K and V codes (d = 4, 256 centroids).
 Timing: W eager warm-up steps; then exactly K steps captured in one CUDA graph
 and replayed between CUDA events, with a barrier and a synchronize on both
 sides (max over ranks).  Step i reads cache copy i % R, R copies together
-larger than twice the L2 cache, so codes come from HBM.  The split kernel is
-bracketed by graph event nodes, which give its average launch duration for the
-roofline.  SM clocks are sampled with nvidia-smi during the load.
+larger than twice the L2 cache, so codes come from HBM.  A second graph of the
+same steps with event nodes around every kernel, replayed after the timed one,
+gives the per-kernel breakdown and the split kernel's average launch duration
+for the roofline.  SM clocks are sampled with nvidia-smi during the load.
 
 --impl reference times the fp64 CPU oracle (the correctness reference) on the
 host cores on a bounded sample of the same workload; it is a deliberately slow
@@ -255,13 +256,36 @@ def workload_config(w, splits, copies):
                    " of codes) > 2x L2" if copies else None)}
 
 
+
+# ------------------------------------------------------------- multi-rank ---
+# Replicas only: every rank runs the same per-GPU workload with no data-path
+# collective; the job's time is the slowest rank's.
+
+def rank_env():
+    """(rank, world size, local rank) from the torchrun environment."""
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def max_over_ranks(x, dist, device):
+    """The maximum of the per-rank value x over all ranks (x itself without a group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, units_per_rank, ms):
+    """Whole-job throughput: the units all ranks processed per second of the slowest rank."""
+    return world * units_per_rank / (ms / 1e3)
+
 # ----------------------------------------------------------------- our arm ---
 
 def main():
     args = parse()
-    rank = int(os.environ.get("RANK", 0))
-    world = int(os.environ.get("WORLD_SIZE", 1))
-    local = int(os.environ.get("LOCAL_RANK", 0))
+    rank, world, local = rank_env()
     w = W.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w, rank)
@@ -360,22 +384,32 @@ def main():
     assert int(status.item()) == 0, f"device status {int(status.item())}"
 
     K = args.steps
+    cap = torch.cuda.Stream(device=dev)
+
+    def capture(fn, n):
+        gr = torch.cuda.CUDAGraph()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(gr, stream=cap):
+                for i in range(n):
+                    fn(i)
+        torch.cuda.current_stream().wait_stream(cap)
+        gr.replay()
+        torch.cuda.synchronize()
+        return gr
+
+    # The timed graph holds the K steps only; a second graph with event nodes
+    # around every kernel gives the per-kernel breakdown and the split kernel's
+    # launch duration for the roofline.
+    g = capture(step, K)
+    n_ev = min(K, 500)
     try:
         evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
-               for _ in range(K)]
+               for _ in range(n_ev)]
+        g_ev = capture(lambda i: step(i, evs[i]), n_ev)
         graph_events = True
-    except TypeError:
-        evs, graph_events = None, False
-    g = torch.cuda.CUDAGraph()
-    cap = torch.cuda.Stream(device=dev)
-    cap.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(cap):
-        with torch.cuda.graph(g, stream=cap):
-            for i in range(K):
-                step(i, evs[i] if graph_events else None)
-    torch.cuda.current_stream().wait_stream(cap)
-    g.replay()
-    torch.cuda.synchronize()
+    except (TypeError, RuntimeError):
+        evs, g_ev, graph_events = None, None, False
 
     # ---- soak (untimed) so clocks settle, then the timed replay ----------------
     sampler = ClockSampler(device_id_for_smi(torch, local))
@@ -392,18 +426,16 @@ def main():
     torch.cuda.synchronize()
     barrier()
     clocks = sampler.stop()
-    total_ms = t0.elapsed_time(t1)
-    if dist is not None:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(t0.elapsed_time(t1), dist, dev)
     ms_per_step = total_ms / K
 
     if graph_events:
+        g_ev.replay()
+        torch.cuda.synchronize()
         split_ms = [e[1].elapsed_time(e[2]) for e in evs]
         append_ms = [e[0].elapsed_time(e[1]) for e in evs]
         comb_ms = [e[2].elapsed_time(e[3]) for e in evs]
-        timing_note = "graph event nodes around each kernel in the timed replay"
+        timing_note = "graph event nodes around each kernel (a replay after the timed one)"
     else:  # eager fallback: events around each launch after the timed region
         ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(min(K, 500))]
         for i, e in enumerate(ev2):
@@ -417,7 +449,7 @@ def main():
     assert int(status.item()) == 0, f"device status {int(status.item())}"
 
     toks = tokens_per_step(w)
-    value = world * toks / (ms_per_step / 1e3)
+    value = job_rate(world, toks, ms_per_step)
     hbm_peak, peak_src = measured_hbm()
     achieved = step_bytes / (split_avg / 1e3) / 1e9
     traffic = recorded_traffic(args.workload)
@@ -437,26 +469,15 @@ def main():
             step(i)
             out_p.copy_(out, non_blocking=True)
 
-        ge = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(cap):
-            with torch.cuda.graph(ge, stream=cap):
-                for i in range(K):
-                    e2e_step(i)
-        torch.cuda.current_stream().wait_stream(cap)
-        ge.replay()
-        torch.cuda.synchronize()
+        ge = capture(e2e_step, K)
         barrier()
         a, bb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         ge.replay()
         bb.record()
         torch.cuda.synchronize()
-        e_ms = a.elapsed_time(bb) / K
-        if dist is not None:
-            tt = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e_ms = float(tt.item())
-        e2e = {"value": world * toks / (e_ms / 1e3), "unit": UNIT,
+        e_ms = max_over_ranks(a.elapsed_time(bb) / K, dist, dev)
+        e2e = {"value": job_rate(world, toks, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": q_p.numel() * 2 + k_p.numel() * 2 + v_p.numel() * 2,
                "d2h_bytes_per_step": out_p.numel() * 2, "ms_per_step": e_ms}
 
