@@ -28,7 +28,7 @@ VQ_ERR_WORKSPACE = -3
 VQ_ERR_CUDA = -4
 STATUS_NAMES = {0: "VQ_OK", -1: "VQ_ERR_INVALID_ARG", -2: "VQ_ERR_UNSUPPORTED",
                 -3: "VQ_ERR_WORKSPACE", -4: "VQ_ERR_CUDA"}
-VQ_DEV_OK, VQ_DEV_BAD_PAGE, VQ_DEV_BAD_SLOT, VQ_DEV_TIMEOUT = 0, 1, 2, 3
+VQ_DEV_OK, VQ_DEV_BAD_PAGE, VQ_DEV_BAD_SLOT, VQ_DEV_TIMEOUT, VQ_DEV_BAD_CONFIG = 0, 1, 2, 3, 4
 
 # every symbol include/vqattn.h declares
 EXPORTED = ("vq_code_row_bytes", "vq_check_layout", "vq_encode_kv", "vq_decode_workspace_bytes",

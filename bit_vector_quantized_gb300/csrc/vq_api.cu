@@ -286,24 +286,44 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
   p.qscale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 / std::sqrt(128.0));
 
   const int optin = device_smem_optin();
-  // consumer shape: 12 warps x 1 chunk for G <= 4, 8 warps x 1 chunk for
-  // G > 4 (register budget); VQ_DECODE_SHAPE=8x1|8x2|12x1 overrides (a tuning
-  // switch for profiling the shapes).
+  // Pipeline stages: the most (up to 8) that fit, and never fewer than the
+  // producer warps.  A producer waits for its slot to be released by the
+  // parity of the slot's "empty" barrier, which tells adjacent phases apart
+  // only; with at least as many stages as producer warps, the producer's own
+  // previous stage guarantees the barrier is at most one phase behind.
+  auto stages_for = [&](const vqk::DecodeShape& sh, size_t& bytes) {
+    int ns = 8;
+    for (; ns >= vqk::kProducerWarps; --ns) {
+      bytes = vqk::decode_smem(L.k_bits, L.v_bits, p.group, p.k_row, p.v_row, ns, sh.warps,
+                               sh.stage_tok()).total;
+      if (optin <= 0 || bytes <= static_cast<size_t>(optin)) return ns;
+    }
+    return 0;
+  };
+  // Consumer shape: 12 warps x 1 chunk for G <= 4, 8 warps x 1 chunk for
+  // G > 4 (register budget), and 8 x 1 wherever 12 x 1 leaves room for fewer
+  // than kProducerWarps stages; VQ_DECODE_SHAPE=8x1|8x2|12x1 selects a shape
+  // explicitly (a tuning switch for profiling; an explicit shape that does not
+  // fit is an error).
   vqk::DecodeShape shape = p.group > 4 ? vqk::DecodeShape{8, 1} : vqk::DecodeShape{12, 1};
+  bool explicit_shape = false;
   if (const char* env = std::getenv("VQ_DECODE_SHAPE")) {
-    if (std::strcmp(env, "8x2") == 0) shape = vqk::DecodeShape{8, 2};
-    if (std::strcmp(env, "8x1") == 0) shape = vqk::DecodeShape{8, 1};
-    if (std::strcmp(env, "12x1") == 0) shape = vqk::DecodeShape{12, 1};
+    if (std::strcmp(env, "8x2") == 0) shape = vqk::DecodeShape{8, 2}, explicit_shape = true;
+    if (std::strcmp(env, "8x1") == 0) shape = vqk::DecodeShape{8, 1}, explicit_shape = true;
+    if (std::strcmp(env, "12x1") == 0) shape = vqk::DecodeShape{12, 1}, explicit_shape = true;
   }
+  int nstage = stages_for(shape, smem);
+  if (nstage == 0 && !explicit_shape && shape.warps != 8) {
+    shape = vqk::DecodeShape{8, 1};
+    nstage = stages_for(shape, smem);
+  }
+  if (nstage == 0)
+    return fail(VQ_ERR_UNSUPPORTED,
+                "decode pipeline does not fit: %d consumer warps x %d chunks need %zu bytes of shared "
+                "memory for %d stages",
+                shape.warps, shape.chunks, smem, vqk::kProducerWarps);
   p.warps = shape.warps;
   p.chunks = shape.chunks;
-  int nstage = 8;  // pipeline stages: the largest power of two that fits
-  for (; nstage >= 2; nstage /= 2) {
-    smem = vqk::decode_smem(L.k_bits, L.v_bits, p.group, p.k_row, p.v_row, nstage, shape.warps,
-                            shape.stage_tok()).total;
-    if (optin <= 0 || smem <= static_cast<size_t>(optin)) break;
-  }
-  if (nstage < 2) return fail(VQ_ERR_UNSUPPORTED, "decode shared memory does not fit (%zu bytes)", smem);
   p.nstage = nstage;
   return VQ_OK;
 }

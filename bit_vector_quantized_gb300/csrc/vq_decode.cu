@@ -53,26 +53,27 @@ namespace vqk {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
+constexpr float kLazyLog2 = 8.f;  // running-max slack of the online softmax (log2 units)
 
-// Shared-memory gathers from the read-only codebook replicas (32-bit addresses).
-__device__ __forceinline__ uint2 gather64(uint32_t a) {
-  uint2 v;
-  asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
-  return v;
+// The dynamic shared memory of the split kernel; the codebook table sits at
+// its start (offset 0), so a gather is one load at (code << 8) | lane byte.
+extern __shared__ __align__(128) uint8_t g_smem[];
+
+__device__ __forceinline__ uint2 tab64(uint32_t off) {
+  return *reinterpret_cast<const uint2*>(g_smem + off);
 }
-__device__ __forceinline__ uint32_t gather32(uint32_t a) {
-  uint32_t v;
-  asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-  return v;
+__device__ __forceinline__ uint32_t tab32(uint32_t off) {
+  return *reinterpret_cast<const uint32_t*>(g_smem + off);
 }
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// Byte i of w, scaled by the 128-byte replica row stride.
-__device__ __forceinline__ uint32_t row_of_byte(uint32_t w, int i) {
-  return __byte_perm(w, 0, 0x4440 | i) << 7;
+// Table offset of the 8-bit code in byte i of w: byte 1 of the result is the
+// code (the 256-byte row), byte 0 the lane's byte inside the row (lw < 256).
+__device__ __forceinline__ uint32_t row_addr(uint32_t w, uint32_t lw, int i) {
+  return __byte_perm(w, lw, 0x5504 | (i << 4));
 }
 
 // K codes of one token for the lane's 8 (dk = 4) or 16 (dk = 2) sub-vectors.
@@ -84,7 +85,9 @@ struct KCodes<4> {
   __device__ __forceinline__ void load(const uint8_t* row, int c) {
     w = *reinterpret_cast<const uint2*>(row + 8 * c);
   }
-  __device__ __forceinline__ uint32_t off(int i) const { return row_of_byte(i < 4 ? w.x : w.y, i & 3); }
+  __device__ __forceinline__ uint32_t off(int i, uint32_t lw) const {
+    return row_addr(i < 4 ? w.x : w.y, lw, i & 3);
+  }
 };
 template <>
 struct KCodes<2> {
@@ -92,9 +95,9 @@ struct KCodes<2> {
   __device__ __forceinline__ void load(const uint8_t* row, int c) {
     w = *reinterpret_cast<const uint4*>(row + 16 * c);
   }
-  __device__ __forceinline__ uint32_t off(int i) const {
+  __device__ __forceinline__ uint32_t off(int i, uint32_t lw) const {
     const uint32_t v = i < 4 ? w.x : i < 8 ? w.y : i < 12 ? w.z : w.w;
-    return row_of_byte(v, i & 3);
+    return row_addr(v, lw, i & 3);
   }
 };
 
@@ -108,21 +111,22 @@ struct VCodes<4, 8> {
   __device__ __forceinline__ void load(const uint8_t* row, int r) {
     w = *reinterpret_cast<const uint32_t*>(row + 4 * r);
   }
-  __device__ __forceinline__ uint32_t off(int i) const { return row_of_byte(w, i); }
+  __device__ __forceinline__ uint32_t off(int i, uint32_t lw) const { return row_addr(w, lw, i); }
 };
 template <>
 struct VCodes<4, 9> {
-  uint32_t lo, hi;
-  int sh;
+  uint32_t a, b;  // the lane's 36-bit code group: bits 0..31 in a, 32..35 in b
   __device__ __forceinline__ void load(const uint8_t* row, int r) {
     // codes 4r .. 4r+3 sit at bits 36r .. 36r+35: words r and r+1, shift 4r
-    lo = *reinterpret_cast<const uint32_t*>(row + 4 * r);
-    hi = *reinterpret_cast<const uint32_t*>(row + 4 * r + 4);
-    sh = 4 * r;
+    const uint32_t lo = *reinterpret_cast<const uint32_t*>(row + 4 * r);
+    const uint32_t hi = *reinterpret_cast<const uint32_t*>(row + 4 * r + 4);
+    a = __funnelshift_r(lo, hi, 4 * r);
+    b = hi >> (4 * r);
   }
-  __device__ __forceinline__ uint32_t off(int i) const {
-    const uint64_t w = (static_cast<uint64_t>(hi) << 32) | lo;
-    return (static_cast<uint32_t>(w >> (sh + 9 * i)) & 0x1ffu) << 7;
+  __device__ __forceinline__ uint32_t off(int i, uint32_t lw) const {
+    // code i = group bits 9i .. 9i+8, moved to bits 8..16 (the table row)
+    const uint32_t x = i == 0 ? a << 8 : i == 1 ? a >> 1 : i == 2 ? a >> 10 : __funnelshift_r(a, b, 19);
+    return (x & 0x1ff00u) | lw;
   }
 };
 template <>
@@ -131,7 +135,9 @@ struct VCodes<2, 8> {
   __device__ __forceinline__ void load(const uint8_t* row, int r) {
     w = *reinterpret_cast<const uint2*>(row + 8 * r);
   }
-  __device__ __forceinline__ uint32_t off(int i) const { return row_of_byte(i < 4 ? w.x : w.y, i & 3); }
+  __device__ __forceinline__ uint32_t off(int i, uint32_t lw) const {
+    return row_addr(i < 4 ? w.x : w.y, lw, i & 3);
+  }
 };
 
 struct UnitId {
@@ -193,9 +199,9 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   constexpr int NP = kProducerWarps;
   constexpr int kSlice = kNCH * kChunk;      // tokens per consumer warp per stage
   constexpr int kStageTok = NW * kSlice;     // tokens per pipeline stage
-  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* const smem = g_smem;
   const int G = p.group;
-  const int NS = p.nstage;  // power of two
+  const int NS = p.nstage;  // kProducerWarps .. 8 stages
   const DecodeSmem L = decode_smem(BK, BV, G, p.k_row, p.v_row, NS, NW, kStageTok);
   float* qt = reinterpret_cast<float*>(smem + L.qt);
   float* merge = reinterpret_cast<float*>(smem + L.merge);
@@ -210,11 +216,14 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int stage_bytes = kStageTok * (p.k_row + p.v_row);
-  const int ns_shift = __ffs(NS) - 1;
   const int n_units = (p.num_units - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                       static_cast<int>(gridDim.x);
   auto clamp_len = [&](int len) { return len < 0 ? 0 : (len > p.max_seq_len ? p.max_seq_len : len); };
 
+  if (NS < NP || NS > 8) {  // the slot hand-off needs NS >= NP (the host never launches otherwise)
+    if (tid == 0) report(p.status, kDevBadConfig);
+    return;
+  }
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(full + i, 1);
@@ -286,7 +295,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       return pi < p.max_pages ? __ldg(p.page_table + static_cast<long long>(it.u.b) * p.max_pages + pi) : -1;
     };
     auto issue = [&](const UnitStages& su, int sj, int page, int n) {
-      const int slot = n & (NS - 1);
+      const int slot = n % NS;
       const int t0 = su.t_begin + sj * kStageTok;
       const int tend = min(t0 + kStageTok, su.t_end);
       const Piece pc = piece_of(su, sj);
@@ -340,9 +349,9 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         if (cur.k >= n_units || stop) break;
-        const int slot = n & (NS - 1);
+        const int slot = n % NS;
         if (n >= NS) {  // wait until the consumers have released the slot
-          const uint32_t par = static_cast<uint32_t>((n >> ns_shift) - 1) & 1u;
+          const uint32_t par = static_cast<uint32_t>(n / NS - 1) & 1u;
           bool ok = !*abort_flag && mbar_wait_bounded(empty + slot, par, abort_flag, p.timeout_ns);
           ok = __all_sync(kFull, ok);
           if (!ok) {
@@ -365,7 +374,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
     if (*abort_flag && lane == 0) {  // wait (bounded) for this warp's copies still in flight
       for (int i = n - NP; i >= 0 && i >= n - NS - NP; i -= NP) {
         volatile int no_abort = 0;
-        mbar_wait_bounded(full + (i & (NS - 1)), static_cast<uint32_t>(i >> ns_shift) & 1u, &no_abort,
+        mbar_wait_bounded(full + i % NS, static_cast<uint32_t>(i / NS) & 1u, &no_abort,
                           p.timeout_ns);
       }
     }
@@ -407,8 +416,9 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
     }
   };
   load_q(0);
-  {  // codebook replicas: 8-byte centroid j -> 16 copies at j*128 + copy*8; 4-byte -> 32 at j*128 + copy*4
-    const uint32_t cbk = smem_addr(smem + L.cbk), cbv = smem_addr(smem + L.cbv);
+  {  // codebook table: row j = 16 copies of 8-byte (32 copies of 4-byte) K centroid j,
+     // then the same for V centroid j
+    const uint32_t tab = smem_addr(smem + L.tab);
 #pragma unroll
     for (int i = 0; i < kNK; ++i) {
       const int j = tid + i * kConsumerThreads;
@@ -416,12 +426,12 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
         if constexpr (DK == 4) {
 #pragma unroll
           for (int rep = 0; rep < 16; ++rep)
-            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(cbk + j * 128 + rep * 8),
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(tab + j * kTabRow + rep * 8),
                          "r"(cbk_r[i].x), "r"(cbk_r[i].y));
         } else {
 #pragma unroll
           for (int rep = 0; rep < 32; ++rep)
-            asm volatile("st.shared.u32 [%0], %1;" ::"r"(cbk + j * 128 + rep * 4), "r"(cbk_r[i].x));
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(tab + j * kTabRow + rep * 4), "r"(cbk_r[i].x));
         }
       }
     }
@@ -432,12 +442,12 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
         if constexpr (DV == 4) {
 #pragma unroll
           for (int rep = 0; rep < 16; ++rep)
-            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(cbv + j * 128 + rep * 8),
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(tab + j * kTabRow + 128 + rep * 8),
                          "r"(cbv_r[i].x), "r"(cbv_r[i].y));
         } else {
 #pragma unroll
           for (int rep = 0; rep < 32; ++rep)
-            asm volatile("st.shared.u32 [%0], %1;" ::"r"(cbv + j * 128 + rep * 4), "r"(cbv_r[i].x));
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(tab + j * kTabRow + 128 + rep * 4), "r"(cbv_r[i].x));
         }
       }
     }
@@ -446,8 +456,10 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   consumer_sync<NW>();  // codebooks and unit lengths visible to the consumers
 
   const int r = lane >> 2, c = lane & 3;
-  const uint32_t cbk_lane = smem_addr(smem + L.cbk) + (DK == 4 ? (lane & 15) * 8 : lane * 4);
-  const uint32_t cbv_lane = smem_addr(smem + L.cbv) + (DV == 4 ? (lane & 15) * 8 : lane * 4);
+  // the lane's byte inside a table row: its replica of the K (bytes 0..127)
+  // or V (bytes 128..255) centroid, one bank pair (8-byte) or bank (4-byte) per lane
+  const uint32_t lwk = DK == 4 ? (lane & 15) * 8 : lane * 4;
+  const uint32_t lwv = 128 + (DV == 4 ? (lane & 15) * 8 : lane * 4);
   uint32_t qa[8][2];  // score B operands: NG == 4: columns (2g: hi, 2g+1: lo); NG == 8: hi
   uint32_t qb[8][2];  // NG == 8: lo
   float O[8][4];      // output accumulators (NG == 4 uses O[0..3])
@@ -501,14 +513,14 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
         for (int ks = 0; ks < 2; ++ks) {  // tokens 8ks + c and 8ks + c + 4
           uint32_t a0, a1, a2, a3;
           if constexpr (DV == 4) {
-            const uint2 w0 = gather64(cbv_lane + pvc[n][2 * ks].off(q));
-            const uint2 w1 = gather64(cbv_lane + pvc[n][2 * ks + 1].off(q));
+            const uint2 w0 = tab64(pvc[n][2 * ks].off(q, lwv));
+            const uint2 w1 = tab64(pvc[n][2 * ks + 1].off(q, lwv));
             a0 = w0.x; a1 = w0.y; a2 = w1.x; a3 = w1.y;
           } else {
-            a0 = gather32(cbv_lane + pvc[n][2 * ks].off(2 * q));
-            a1 = gather32(cbv_lane + pvc[n][2 * ks].off(2 * q + 1));
-            a2 = gather32(cbv_lane + pvc[n][2 * ks + 1].off(2 * q));
-            a3 = gather32(cbv_lane + pvc[n][2 * ks + 1].off(2 * q + 1));
+            a0 = tab32(pvc[n][2 * ks].off(2 * q, lwv));
+            a1 = tab32(pvc[n][2 * ks].off(2 * q + 1, lwv));
+            a2 = tab32(pvc[n][2 * ks + 1].off(2 * q, lwv));
+            a3 = tab32(pvc[n][2 * ks + 1].off(2 * q + 1, lwv));
           }
           mma16816(O[q], a0, a1, a2, a3, pb[n][ks][0], pb[n][ks][1]);
         }
@@ -516,7 +528,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
         if constexpr (DV == 4) {  // q = output step pair (2q, 2q+1)
           uint2 W[4];
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) W[jj] = gather64(cbv_lane + pvc[n][jj].off(q));
+          for (int jj = 0; jj < 4; ++jj) W[jj] = tab64(pvc[n][jj].off(q, lwv));
           mma16816(O[2 * q], __byte_perm(W[0].x, W[1].x, sel_lo), __byte_perm(W[0].x, W[1].x, sel_hi),
                    __byte_perm(W[2].x, W[3].x, sel_lo), __byte_perm(W[2].x, W[3].x, sel_hi), pb[n][0][0],
                    pb[n][0][1]);
@@ -528,7 +540,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
           for (int h = 0; h < 2; ++h) {
             uint32_t W[4];
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) W[jj] = gather32(cbv_lane + pvc[n][jj].off(2 * q + h));
+            for (int jj = 0; jj < 4; ++jj) W[jj] = tab32(pvc[n][jj].off(2 * q + h, lwv));
             mma16816(O[2 * q + h], __byte_perm(W[0], W[1], 0x5410), __byte_perm(W[0], W[1], 0x7632),
                      __byte_perm(W[2], W[3], 0x5410), __byte_perm(W[2], W[3], 0x7632), pb[n][0][0],
                      pb[n][0][1]);
@@ -555,14 +567,14 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
         for (int n = 0; n < kNCH; ++n) {
           uint32_t a0, a1, a2, a3;
           if constexpr (DK == 4) {
-            const uint2 g0 = gather64(cbk_lane + kc[n][0].off(kk));
-            const uint2 g1 = gather64(cbk_lane + kc[n][1].off(kk));
+            const uint2 g0 = tab64(kc[n][0].off(kk, lwk));
+            const uint2 g1 = tab64(kc[n][1].off(kk, lwk));
             a0 = g0.x; a1 = g1.x; a2 = g0.y; a3 = g1.y;
           } else {
-            a0 = gather32(cbk_lane + kc[n][0].off(2 * kk));
-            a1 = gather32(cbk_lane + kc[n][1].off(2 * kk));
-            a2 = gather32(cbk_lane + kc[n][0].off(2 * kk + 1));
-            a3 = gather32(cbk_lane + kc[n][1].off(2 * kk + 1));
+            a0 = tab32(kc[n][0].off(2 * kk, lwk));
+            a1 = tab32(kc[n][1].off(2 * kk, lwk));
+            a2 = tab32(kc[n][0].off(2 * kk + 1, lwk));
+            a3 = tab32(kc[n][1].off(2 * kk + 1, lwk));
           }
           mma16816(acc[n][kk & 1], a0, a1, a2, a3, qa[kk][0], qa[kk][1]);
           if constexpr (NG == 8) mma16816(acc2[n][kk & 1], a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
@@ -598,32 +610,33 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
         s[n][1][1] = t1 < lim_n ? sc[n][3] : -INFINITY;
       }
     }
-    float alpha[NGL];
-    bool rescale = false;
+    // Lazy running max: m_run moves only when a score exceeds it by more than
+    // kLazyLog2, so p = 2^(s - m_run) <= 2^kLazyLog2 stays far inside fp16 and
+    // fp32 range, and most chunks skip the warp max reduction and the rescale
+    // of O and l.  Any common reference gives the same normalised result.
+    float lmax[NGL];
+    bool grow = false;
 #pragma unroll
     for (int gi = 0; gi < NGL; ++gi) {
       float mx = -INFINITY;
 #pragma unroll
       for (int n = 0; n < kNCH; ++n) mx = fmaxf(mx, fmaxf(s[n][gi][0], s[n][gi][1]));
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-      const float mnew = fmaxf(m_run[gi], mx);
-      const float mref = mnew == -INFINITY ? 0.f : mnew;
-      alpha[gi] = fast_exp2(m_run[gi] - mref);
-      rescale = rescale || alpha[gi] != 1.f;
-      float lsum = 0.f;
-#pragma unroll
-      for (int n = 0; n < kNCH; ++n)
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          s[n][gi][t] = fast_exp2(s[n][gi][t] - mref);
-          lsum += s[n][gi][t];
-        }
-      l_run[gi] = l_run[gi] * alpha[gi] + lsum;
-      m_run[gi] = mnew;
+      lmax[gi] = mx;
+      grow = grow || mx > m_run[gi] + kLazyLog2;
     }
-    if (__any_sync(kFull, rescale)) {
+    if (__any_sync(kFull, grow)) {
+      float alpha[NGL];
+#pragma unroll
+      for (int gi = 0; gi < NGL; ++gi) {
+        float mx = lmax[gi];
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+        const float mnew = fmaxf(m_run[gi], mx);
+        alpha[gi] = mnew == -INFINITY ? 1.f : fast_exp2(m_run[gi] - mnew);  // 0 from -inf
+        l_run[gi] *= alpha[gi];
+        m_run[gi] = mnew;
+      }
       if constexpr (NG == 4) {
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -636,6 +649,19 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
           O[i][1] *= alpha[NGL - 1]; O[i][3] *= alpha[NGL - 1];
         }
       }
+    }
+#pragma unroll
+    for (int gi = 0; gi < NGL; ++gi) {
+      const float mref = m_run[gi] == -INFINITY ? 0.f : m_run[gi];
+      float lsum = 0.f;
+#pragma unroll
+      for (int n = 0; n < kNCH; ++n)
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          s[n][gi][t] = fast_exp2(s[n][gi][t] - mref);
+          lsum += s[n][gi][t];
+        }
+      l_run[gi] += lsum;
     }
 #pragma unroll
     for (int n = 0; n < kNCH; ++n) {
@@ -660,7 +686,8 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
     }
   };
 
-  int n = 0;  // stages consumed (same sequence as the producers')
+  int slot = 0;          // slot of the next stage (stages run in the producers' order)
+  uint32_t phase = 0u;   // parity of the slot's current fill
   for (int k = 0; k < n_units; ++k) {
     const UnitStages u = unit_stages<kStageTok>(p, k, ulen_c[k]);
     consumer_sync<NW>();  // previous unit's merge buffers and q~ are free
@@ -712,11 +739,8 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       for (int jj = 0; jj < 4; ++jj) pvc[nn][jj] = VCodes<DV, BV>{};
     }
 
-    for (int j = 0; j < u.count; ++j, ++n) {
-      const int slot = n & (NS - 1);
-      bool ok = !*abort_flag &&
-                mbar_wait_bounded(full + slot, static_cast<uint32_t>(n >> ns_shift) & 1u, abort_flag,
-                                  p.timeout_ns);
+    for (int j = 0; j < u.count; ++j) {
+      bool ok = !*abort_flag && mbar_wait_bounded(full + slot, phase, abort_flag, p.timeout_ns);
       ok = __all_sync(kFull, ok);
       if (!ok && lane == 0 && !*abort_flag) {
         *abort_flag = 1;
@@ -729,6 +753,10 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       load_codes(stages + static_cast<size_t>(slot) * stage_bytes, off);
       __syncwarp();
       if (lane == 0) mbar_arrive(empty + slot);  // codes are in registers: the slot may be refilled
+      if (++slot == NS) {
+        slot = 0;
+        phase ^= 1u;
+      }
       float sc[kNCH][4];
       fused(sc, true);                           // scores now, P.V of the previous stage
       // tokens past the end, and chunks whose page was invalid, get p = 0

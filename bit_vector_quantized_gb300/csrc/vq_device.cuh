@@ -13,7 +13,9 @@ namespace vqk {
 constexpr int kHeadDim = 128;
 constexpr int kChunk = 16;  // tokens per mma row block
 
-enum DeviceStatus : int32_t { kDevOk = 0, kDevBadPage = 1, kDevBadSlot = 2, kDevTimeout = 3 };
+enum DeviceStatus : int32_t {
+  kDevOk = 0, kDevBadPage = 1, kDevBadSlot = 2, kDevTimeout = 3, kDevBadConfig = 4
+};
 
 __device__ __forceinline__ void report(int32_t* status, int32_t code) {
   if (status) atomicCAS(status, 0, code);
@@ -44,14 +46,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// One bounded wait for phase `parity` of `bar`: the warp may be suspended by
+// the hardware until the phase completes or about `suspend_ns` nanoseconds
+// pass, whichever comes first; true when the phase completed.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity,
+                                              uint32_t suspend_ns = 0x10000u) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(suspend_ns)
       : "memory");
   return ok != 0;
 }
@@ -63,18 +69,18 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // Waits for phase `parity` of `bar` to complete, giving up after `timeout_ns`
-// nanoseconds (or at once when *abort is set by another warp).  Returns false
-// when it gave up; the caller then treats the stage as empty.
+// nanoseconds (or soon after *abort is set by another warp).  Each try may
+// park the warp for up to ~65 us, so a waiting warp costs almost no issue
+// slots.  Returns false when it gave up; the caller then treats the stage as
+// empty.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort, uint64_t timeout_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > timeout_ns) return false;
-    }
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > timeout_ns) return false;
   }
 }
 

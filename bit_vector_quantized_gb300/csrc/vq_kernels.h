@@ -68,10 +68,15 @@ struct DecodeShape {
 };
 
 // Shared-memory carve-up of the split attention kernel (bytes, 128-aligned);
-// `warps` is the number of consumer warps.
+// `warps` is the number of consumer warps.  The codebook table comes first (at
+// offset 0 of the dynamic shared memory): row j is 256 bytes, the replicas of K
+// centroid j in bytes 0..127 and those of V centroid j in bytes 128..255, so a
+// gather address is (code << 8) | lane byte.
 struct DecodeSmem {
-  int cbk, cbv, qt, merge, ml, units, meta, bar, flag, stage, total;
+  int tab, qt, merge, ml, units, meta, bar, flag, stage, total;
 };
+
+constexpr int kTabRow = 256;  // bytes per codebook table row
 
 __host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
 
@@ -79,8 +84,8 @@ __host__ __device__ inline DecodeSmem decode_smem(int k_bits, int v_bits, int gr
                                                   int v_row, int nstage, int warps, int stage_tok) {
   DecodeSmem s;
   int o = 0;
-  s.cbk = o; o = align128(o + (1 << k_bits) * 128);
-  s.cbv = o; o = align128(o + (1 << v_bits) * 128);
+  const int rows = 1 << (k_bits > v_bits ? k_bits : v_bits);
+  s.tab = o; o = align128(o + rows * kTabRow);
   s.qt = o; o = align128(o + group * 128 * 4);
   s.merge = o; o = align128(o + warps * group * 128 * 4);
   s.ml = o; o = align128(o + warps * group * 8);

@@ -61,7 +61,9 @@ typedef enum vq_device_status {
   VQ_DEV_OK = 0,
   VQ_DEV_BAD_PAGE = 1,       /* page_table entry outside [0, num_pages): page skipped */
   VQ_DEV_BAD_SLOT = 2,       /* slot_mapping entry >= num_pages * page_size: token skipped */
-  VQ_DEV_TIMEOUT = 3         /* an asynchronous-copy wait exceeded its time limit */
+  VQ_DEV_TIMEOUT = 3,        /* an asynchronous-copy wait exceeded its time limit */
+  VQ_DEV_BAD_CONFIG = 4      /* launch parameters the kernel cannot honour: it did nothing
+                                (not reachable through this ABI's validated calls) */
 } vq_device_status;
 
 /*
