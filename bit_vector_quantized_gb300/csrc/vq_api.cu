@@ -280,6 +280,9 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
   p.max_seq_len = max_seq_len;
   p.splits = splits;
   p.num_units = static_cast<int>(units);
+  const int nsl = (max_seq_len + vqk::kUnitTok - 1) / vqk::kUnitTok;
+  p.split_q = nsl / splits;
+  p.split_r = nsl % splits;
   p.k_row = static_cast<int>(vq_code_row_bytes(L.head_dim, L.k_sub, L.k_bits));
   p.v_row = static_cast<int>(vq_code_row_bytes(L.head_dim, L.v_sub, L.v_bits));
   const float scale = softmax_scale == 0.f ? 1.f / std::sqrt(static_cast<float>(L.head_dim)) : softmax_scale;

@@ -168,7 +168,7 @@ __device__ __forceinline__ void consumer_sync() {
 
 // Pipeline stages of one work unit.  A unit covers 32-token blocks [a, b) of
 // its sequence (split boundaries from max_seq_len), clipped to the sequence
-// length; stage j holds its tokens [t0, tend) with t0 = 32 a + 256 j.
+// length; stage j holds its tokens [t0, tend) with t0 = 32 a + kStageTok j.
 struct UnitStages {
   int b, kvh, s, len, t_begin, t_end, count;
 };
@@ -176,9 +176,10 @@ struct UnitStages {
 template <int kStageTok>
 __device__ __forceinline__ UnitStages unit_stages(const DecodeParams& p, int k, int len) {
   const UnitId id = unit_id(p, k);
-  const int nsl = (p.max_seq_len + kUnitTok - 1) / kUnitTok;
-  const int a = static_cast<int>(static_cast<long long>(id.s) * nsl / p.splits);
-  const int b = static_cast<int>(static_cast<long long>(id.s + 1) * nsl / p.splits);
+  // split s covers 32-token blocks [s q + min(s, r), (s + 1) q + min(s + 1, r)) of the
+  // max_seq_len / 32 blocks (q, r: their quotient and remainder by the split count)
+  const int a = id.s * p.split_q + min(id.s, p.split_r);
+  const int b = a + p.split_q + (id.s < p.split_r ? 1 : 0);
   UnitStages u;
   u.b = id.b;
   u.kvh = id.kvh;
@@ -215,12 +216,14 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   uint8_t* stages = smem + L.stage;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();
   const int stage_bytes = kStageTok * (p.k_row + p.v_row);
   const int n_units = (p.num_units - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                       static_cast<int>(gridDim.x);
   auto clamp_len = [&](int len) { return len < 0 ? 0 : (len > p.max_seq_len ? p.max_seq_len : len); };
 
   if (NS < NP || NS > 8) {  // the slot hand-off needs NS >= NP (the host never launches otherwise)
+    pdl_wait();
     if (tid == 0) report(p.status, kDevBadConfig);
     return;
   }
@@ -244,7 +247,14 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
     // issues that piece as one bulk copy.  A warp issuing bulk copies stalls
     // while the copy engine accepts them, so several producer warps together
     // keep enough bytes in flight to reach HBM bandwidth.
+    pdl_wait();  // producers read lengths, page tables and pools
     const int pw = warp - NW;
+    if (pw == 0 && n_units > 0) {  // pull the first unit's page-table entries into L1
+      const UnitId id0 = unit_id(p, 0);
+      const int pg = (id0.s * p.split_q + min(id0.s, p.split_r)) * kUnitTok / p.page_size + lane;
+      if (pg < p.max_pages)
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(p.page_table + static_cast<long long>(id0.b) * p.max_pages + pg));
+    }
     for (int k = tid - NW * 32; k < n_units; k += NP * 32)
       ulen_p[k] = clamp_len(__ldg(p.seq_lens + unit_id(p, k).b));
     producer_sync<NP>();
@@ -402,20 +412,6 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       else cbv_r[i].x = __ldg(reinterpret_cast<const uint32_t*>(p.cb_v) + j);
     }
   }
-  int len_r = 0;
-  if (tid < n_units) len_r = __ldg(p.seq_lens + unit_id(p, tid).b);
-  uint2 q_r = make_uint2(0, 0);
-  float4 lam_r = make_float4(0.f, 0.f, 0.f, 0.f);
-  auto load_q = [&](int k) {  // query and lambda of unit k (consumer warps < G)
-    if (warp < G && k < n_units) {
-      const UnitId id = unit_id(p, k);
-      q_r = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.q) +
-                                               (static_cast<long long>(id.b) * p.hq + id.kvh * G + warp) * kHeadDim) +
-                  lane);
-      lam_r = __ldg(reinterpret_cast<const float4*>(p.lambda + id.kvh * kHeadDim) + lane);
-    }
-  };
-  load_q(0);
   {  // codebook table: row j = 16 copies of 8-byte (32 copies of 4-byte) K centroid j,
      // then the same for V centroid j
     const uint32_t tab = smem_addr(smem + L.tab);
@@ -452,6 +448,21 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       }
     }
   }
+  pdl_wait();  // the codebook table needs only the codebooks; the rest waits for the previous kernel
+  int len_r = 0;
+  if (tid < n_units) len_r = __ldg(p.seq_lens + unit_id(p, tid).b);
+  uint2 q_r = make_uint2(0, 0);
+  float4 lam_r = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto load_q = [&](int k) {  // query and lambda of unit k (consumer warps < G)
+    if (warp < G && k < n_units) {
+      const UnitId id = unit_id(p, k);
+      q_r = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.q) +
+                                               (static_cast<long long>(id.b) * p.hq + id.kvh * G + warp) * kHeadDim) +
+                  lane);
+      lam_r = __ldg(reinterpret_cast<const float4*>(p.lambda + id.kvh * kHeadDim) + lane);
+    }
+  };
+  load_q(0);
   if (tid < n_units) ulen_c[tid] = clamp_len(len_r);
   consumer_sync<NW>();  // codebooks and unit lengths visible to the consumers
 
@@ -826,6 +837,8 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
 __global__ void __launch_bounds__(kHeadDim) vq_combine_kernel(const CombineParams p) {
   extern __shared__ float2 cml[];  // [splits]
   const int row = blockIdx.x, d = threadIdx.x;
+  pdl_trigger();
+  pdl_wait();
   const float2* ml = p.ws_ml + static_cast<long long>(row) * p.splits;
   const float* o = p.ws_o + static_cast<long long>(row) * p.splits * kHeadDim + d;
   for (int s = d; s < p.splits; s += kHeadDim) cml[s] = ml[s];
@@ -864,8 +877,8 @@ cudaError_t launch_split(const DecodeParams& p, int grid, size_t smem, cudaStrea
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  kern<<<grid, (NW + kProducerWarps) * 32, smem, stream>>>(p);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(kern, dim3(grid), dim3((NW + kProducerWarps) * 32), smem, stream, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int DK, int BK, int DV, int BV>
@@ -908,8 +921,8 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  vq_combine_kernel<<<p.rows, kHeadDim, smem, stream>>>(p);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(vq_combine_kernel, dim3(p.rows), dim3(kHeadDim), smem, stream, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace vqk

@@ -25,6 +25,19 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ------------------------------------------- programmatic dependent launch ---
+// The library's kernels are launched with programmatic stream serialization:
+// a kernel may be scheduled while the previous kernel in the stream still runs
+// if that kernel signals pdl_trigger (only the library's own kernels do).
+// Before pdl_wait a kernel reads nothing but the codebooks, which none of the
+// library's kernels writes; pdl_wait blocks until the previous kernel has
+// completed and its memory is visible.  Without the launch attribute both are
+// no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier ---
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kEncWarps * 32) vq_encode_kernel(const EncodeP
   float* cnorm = cmul + ncent * d;        // [ncent]: ||c_j||^2
   float* red_best = cnorm + ((ncent + 3) & ~3);
   int* red_idx = reinterpret_cast<int*>(red_best + kEncWarps * 32 * 4);
-  const VecIn in = load_vector(p, which);
+  pdl_trigger();
   const __half* cb = static_cast<const __half*>(p.cb[which]);
   for (int j = threadIdx.x; j < ncent; j += blockDim.x) {
     float n = 0.f;
@@ -256,6 +256,8 @@ __global__ void __launch_bounds__(kEncWarps * 32) vq_encode_kernel(const EncodeP
     }
     cnorm[j] = n;
   }
+  pdl_wait();  // the codebook table needs only the codebook; the rest waits for the previous kernel
+  const VecIn in = load_vector(p, which);
   __syncthreads();
   switch (d) {
     case 1: encode_vector<1>(p, which, in, cmul, cnorm, red_best, red_idx); break;
@@ -285,8 +287,8 @@ cudaError_t launch_encode(const EncodeParams& p, int grid_x, int grid_y, size_t 
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  vq_encode_kernel<<<dim3(grid_x, grid_y), kEncWarps * 32, smem, stream>>>(p);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(vq_encode_kernel, dim3(grid_x, grid_y), dim3(kEncWarps * 32), smem, stream, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace vqk

@@ -42,6 +42,7 @@ struct DecodeParams {
   int batch, hq, hkv, group;
   int page_size, max_pages, max_seq_len;
   int splits, num_units;
+  int split_q, split_r;       // ceil(max_seq_len / 32) = split_q * splits + split_r
   int k_row, v_row;
   int nstage;
   int warps, chunks;          // consumer shape (DecodeShape)
@@ -96,6 +97,24 @@ __host__ __device__ inline DecodeSmem decode_smem(int k_bits, int v_bits, int gr
   s.stage = o; o = align128(o + nstage * stage_tok * (k_row + v_row));
   s.total = o;
   return s;
+}
+
+// Launches `kern` with programmatic stream serialization (see pdl_wait in
+// vq_device.cuh).
+template <typename Params>
+inline cudaError_t launch_pdl(void (*kern)(Params), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, const Params& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 // Launchers (return the cudaError_t of the launch).
