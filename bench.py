@@ -248,6 +248,23 @@ def run_reference(args, w, rank):
     print(json.dumps(line), flush=True)
 
 
+def encode_report(w, tokens, ms, sms, clocks):
+    """Prefill encode throughput and its roofline.  The encode is bound by the FP32
+    pipe: a nearest-centroid scan spends d fused multiply-adds per centroid and
+    sub-vector, i.e. 2^bits * head_dim per token-head and tensor; the peak is
+    128 FP32 lanes per SM at the sampled SM clock."""
+    th = tokens * w.num_kv_heads
+    fma = th * ((1 << w.k_bits) + (1 << w.v_bits)) * w.head_dim
+    mhz = (clocks or {}).get("sm_mhz") or (clocks or {}).get("sm_max_mhz") or 2070.0
+    peak = sms * 128 * mhz * 1e6
+    achieved = fma / (ms / 1e3)
+    return {"tokens": tokens, "ms": ms, "token_heads_per_s": th / (ms / 1e3),
+            "roofline": {"bound": "alu", "achieved": achieved / 1e12, "peak": peak / 1e12,
+                         "unit": "TFMA/s", "frac": achieved / peak,
+                         "peak_source": f"derived: {sms} SMs x 128 FP32 lanes x {mhz:.0f} MHz",
+                         "algorithmic_fma_per_token_head": ((1 << w.k_bits) + (1 << w.v_bits)) * w.head_dim}}
+
+
 def workload_config(w, splits, copies):
     return {"workload": w.name, "batch": w.batch, "q_heads": w.num_q_heads,
             "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "context": w.context,
@@ -354,6 +371,7 @@ def main():
     out = torch.empty((B, w.num_q_heads, w.head_dim), dtype=torch.float16, device=dev)
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     step_bytes = code_bytes_per_step(w)
     copies = args.copies or max(1, -(-2 * l2 // step_bytes))
     pools = [(k_pool, v_pool)] + [(k_pool.clone(), v_pool.clone()) for _ in range(copies - 1)]
@@ -524,8 +542,7 @@ def main():
                              "split_attention": 1e3 * split_avg,
                              "split_attention_back_to_back": 1e3 * split_launch_ms,
                              "combine": 1e3 * float(np.mean(comb_ms)), "step": 1e3 * ms_per_step},
-            "prefill_encode": {"tokens": prefill_tokens, "ms": enc_ms,
-                               "token_heads_per_s": prefill_tokens * w.num_kv_heads / (enc_ms / 1e3)},
+            "prefill_encode": encode_report(w, prefill_tokens, enc_ms, sms, clocks),
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * K, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -182,7 +182,10 @@ vq_status vq_encode_kv(const vq_layout* layout, int32_t num_tokens, const void* 
   const int sms = device_sms();
   // few vectors (a decode-step append): spread each codebook scan over 8 warps
   p.split = vectors * 2 < static_cast<long long>(sms > 0 ? sms : 148) * 8 ? 8 : 1;
-  const int per_cta = 8 / p.split;
+  // many vectors with sub-vector lengths 2 / 4: several vectors per warp
+  const bool multi_ok = (!k || L.k_sub == 2 || L.k_sub == 4) && (!v || L.v_sub == 2 || L.v_sub == 4);
+  p.vec_per_warp = (p.split == 1 && multi_ok) ? vqk::kMultiVec : 1;
+  const int per_cta = 8 * p.vec_per_warp / p.split;
   const long long grid_x = (vectors + per_cta - 1) / per_cta;
   if (grid_x > 0x7fffffffLL) return fail(VQ_ERR_INVALID_ARG, "too many tokens (%d)", num_tokens);
   p.which_base = k ? 0 : 1;

@@ -134,10 +134,59 @@ __device__ __forceinline__ VecIn load_vector(const EncodeParams& p, int which) {
   return in;
 }
 
+// Packs one vector's codes and stores the row.  Lane w assembles 32-bit word w
+// of the row from the codes that overlap bits [32w, 32w + 32) of the LSB-first
+// stream; idx[s] is the code of the lane's s-th sub-vector.  Every lane of the
+// warp must call it (shuffles); `active` false stores nothing.
+template <int D>
+__device__ __forceinline__ void pack_store(const EncodeParams& p, int which, const int (&idx)[4],
+                                           bool active, int h, long long slot) {
+  constexpr int NS = Scan<D>::kSub;
+  const int lane = threadIdx.x & 31;
+  const int bits = p.bits[which];
+  const int S = kHeadDim / D;
+  const int row_words = p.row_bytes[which] / 4;
+  const int i_lo = (32 * lane) / bits;
+  const int kmax = 32 / bits + 2;
+  uint32_t word = 0;
+  for (int k = 0; k < kmax; ++k) {
+    const int i = i_lo + k;
+    int own, reg;
+    if constexpr (D == 8) {
+      own = 2 * i;
+      reg = 0;
+    } else {
+      own = i / NS;
+      reg = i % NS;
+    }
+    own = own > 31 ? 31 : own;
+    uint32_t v = 0;
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+      const uint32_t tv = __shfl_sync(0xffffffffu, static_cast<uint32_t>(idx[s]), own);
+      if (s == reg) v = tv;
+    }
+    if (i < S) {
+      const int pos = i * bits - 32 * lane;
+      if (pos < 32 && pos > -bits)
+        word |= static_cast<uint32_t>((static_cast<uint64_t>(v) << (pos + 32)) >> 32);
+    }
+  }
+  if (!active || lane >= row_words) return;
+  if (slot < 0) return;  // padding token
+  if (slot >= p.num_slots) {
+    if (lane == 0) report(p.status, kDevBadSlot);
+    return;
+  }
+  const long long page = slot / p.page_size, off = slot % p.page_size;
+  uint8_t* row = p.pool[which] +
+                 ((page * p.hkv + h) * p.page_size + off) * static_cast<long long>(p.row_bytes[which]);
+  reinterpret_cast<uint32_t*>(row)[lane] = word;
+}
+
 template <int D>
 __device__ void encode_vector(const EncodeParams& p, int which, const VecIn& in, const float* cmul,
                               const float* cnorm, float* red_best, int* red_idx) {
-  constexpr int NS = Scan<D>::kSub;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = p.split;
   const int wing = warp % split;
@@ -193,47 +242,106 @@ __device__ void encode_vector(const EncodeParams& p, int which, const VecIn& in,
   }
   if (wing != 0) return;
 
-  // Pack: lane w assembles 32-bit word w of the row from the codes that overlap
-  // bits [32w, 32w + 32) of the LSB-first stream.
-  const int S = kHeadDim / D;
-  const int row_words = p.row_bytes[which] / 4;
-  const int i_lo = (32 * lane) / bits;
-  const int kmax = 32 / bits + 2;
-  uint32_t word = 0;
-  for (int k = 0; k < kmax; ++k) {
-    const int i = i_lo + k;
-    int own, reg;
-    if constexpr (D == 8) {
-      own = 2 * i;
-      reg = 0;
-    } else {
-      own = i / NS;
-      reg = i % NS;
-    }
-    own = own > 31 ? 31 : own;
-    uint32_t v = 0;
+  pack_store<D>(p, which, idx, active, h, in.slot);
+}
+
+// Cache fill of many vectors (prefill): each warp encodes NV consecutive
+// token-head vectors and reads every centroid once for all of them, so the
+// shared-memory loads are amortised and the NV argmin chains run side by side.
+// The score of each (vector, sub-vector, centroid) is computed exactly as in
+// scan_centroids, so the codes are the same.  Sub-vector lengths 2 and 4.
+template <int D, int NV>
+__device__ void encode_multi(const EncodeParams& p, int which, const float* cmul, const float* cnorm) {
+  static_assert(D == 2 || D == 4, "multi-vector scan");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long nvec = static_cast<long long>(p.num_tokens) * p.hkv;
+  const long long base = (static_cast<long long>(blockIdx.x) * kEncWarps + warp) * NV;
+  uint2 raw[NV];
+  float4 lam[NV];
+  bool act[NV];
+  int hh[NV];
+  long long slot[NV];
 #pragma unroll
-    for (int s = 0; s < NS; ++s) {
-      const uint32_t tv = __shfl_sync(0xffffffffu, static_cast<uint32_t>(idx[s]), own);
-      if (s == reg) v = tv;
-    }
-    if (i < S) {
-      const int pos = i * bits - 32 * lane;
-      if (pos < 32 && pos > -bits)
-        word |= static_cast<uint32_t>((static_cast<uint64_t>(v) << (pos + 32)) >> 32);
+  for (int v = 0; v < NV; ++v) {  // every global load of the warp in flight before the barrier
+    const long long th = base + v;
+    act[v] = th < nvec;
+    const long long t = act[v] ? th / p.hkv : 0;
+    hh[v] = act[v] ? static_cast<int>(th % p.hkv) : 0;
+    raw[v] = make_uint2(0, 0);
+    lam[v] = make_float4(1.f, 1.f, 1.f, 1.f);
+    slot[v] = -1;
+    if (act[v]) {
+      raw[v] = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.src[which]) +
+                                                    (t * p.hkv + hh[v]) * kHeadDim) + lane);
+      if (which == 0) lam[v] = __ldg(reinterpret_cast<const float4*>(p.lambda + hh[v] * kHeadDim) + lane);
+      slot[v] = __ldg(p.slots + t);
     }
   }
-  if (!active || lane >= row_words) return;
-  const long long slot = in.slot;
-  if (slot < 0) return;  // padding token
-  if (slot >= p.num_slots) {
-    if (lane == 0) report(p.status, kDevBadSlot);
-    return;
+  __syncthreads();  // the codebook table is ready
+  float x[NV][4];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const __half2 lo = *reinterpret_cast<const __half2*>(&raw[v].x);
+    const __half2 hi = *reinterpret_cast<const __half2*>(&raw[v].y);
+    x[v][0] = __low2float(lo);
+    x[v][1] = __high2float(lo);
+    x[v][2] = __low2float(hi);
+    x[v][3] = __high2float(hi);
+    if (which == 0) {  // keys: smoothing then Walsh-Hadamard
+      x[v][0] = x[v][0] / lam[v].x;
+      x[v][1] = x[v][1] / lam[v].y;
+      x[v][2] = x[v][2] / lam[v].z;
+      x[v][3] = x[v][3] / lam[v].w;
+      fwht128_warp(x[v], lane);
+      const float r = 0.08838834764831845f;  // 1/sqrt(128)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[v][e] *= r;
+    }
   }
-  const long long page = slot / p.page_size, off = slot % p.page_size;
-  uint8_t* row = p.pool[which] +
-                 ((page * p.hkv + h) * p.page_size + off) * static_cast<long long>(p.row_bytes[which]);
-  reinterpret_cast<uint32_t*>(row)[lane] = word;
+  float best[NV][2];
+  int idx[NV][4];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    best[v][0] = best[v][1] = INFINITY;
+    idx[v][0] = idx[v][1] = idx[v][2] = idx[v][3] = 0x7fffffff;
+  }
+  const int ncent = 1 << p.bits[which];
+#pragma unroll 2
+  for (int j = 0; j < ncent; ++j) {
+    const float n = cnorm[j];
+    if constexpr (D == 4) {
+      const float4 c = *reinterpret_cast<const float4*>(cmul + j * 4);
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        float sc = n;
+        sc = fmaf(x[v][0], c.x, sc);
+        sc = fmaf(x[v][1], c.y, sc);
+        sc = fmaf(x[v][2], c.z, sc);
+        sc = fmaf(x[v][3], c.w, sc);
+        if (sc < best[v][0]) {
+          best[v][0] = sc;
+          idx[v][0] = j;
+        }
+      }
+    } else {
+      const float2 c = *reinterpret_cast<const float2*>(cmul + j * 2);
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const float s0 = fmaf(x[v][1], c.y, fmaf(x[v][0], c.x, n));
+        const float s1 = fmaf(x[v][3], c.y, fmaf(x[v][2], c.x, n));
+        if (s0 < best[v][0]) {
+          best[v][0] = s0;
+          idx[v][0] = j;
+        }
+        if (s1 < best[v][1]) {
+          best[v][1] = s1;
+          idx[v][1] = j;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int v = 0; v < NV; ++v) pack_store<D>(p, which, idx[v], act[v], hh[v], slot[v]);
 }
 
 __global__ void __launch_bounds__(kEncWarps * 32) vq_encode_kernel(const EncodeParams p) {
@@ -257,6 +365,11 @@ __global__ void __launch_bounds__(kEncWarps * 32) vq_encode_kernel(const EncodeP
     cnorm[j] = n;
   }
   pdl_wait();  // the codebook table needs only the codebook; the rest waits for the previous kernel
+  if (p.vec_per_warp == kMultiVec) {  // prefill: several vectors per warp (sub-vector length 2 or 4)
+    if (d == 4) encode_multi<4, kMultiVec>(p, which, cmul, cnorm);
+    else encode_multi<2, kMultiVec>(p, which, cmul, cnorm);
+    return;
+  }
   const VecIn in = load_vector(p, which);
   __syncthreads();
   switch (d) {

@@ -23,7 +23,10 @@ struct EncodeParams {
   int page_size;
   int split;             // warps per token-head: 1, 2, 4 or 8
   int which_base;        // blockIdx.y + which_base selects keys (0) or values (1)
+  int vec_per_warp;      // 1, or kMultiVec (prefill with sub-vector lengths 2 / 4; split == 1)
 };
+
+constexpr int kMultiVec = 4;  // vectors per warp of the prefill encode
 
 struct DecodeParams {
   const void* q;              // fp16 [B][Hq][128]
