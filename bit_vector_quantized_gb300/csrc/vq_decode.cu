@@ -247,7 +247,6 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
     // issues that piece as one bulk copy.  A warp issuing bulk copies stalls
     // while the copy engine accepts them, so several producer warps together
     // keep enough bytes in flight to reach HBM bandwidth.
-    pdl_wait();  // producers read lengths, page tables and pools
     const int pw = warp - NW;
     if (pw == 0 && n_units > 0) {  // pull the first unit's page-table entries into L1
       const UnitId id0 = unit_id(p, 0);
@@ -353,6 +352,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       ring[i] = lookup(ahead);
       skip(ahead);
     }
+    pdl_wait();  // the pools may be written by the previous kernel: copy only after it
     int n = pw;
     bool stop = false;
     while (cur.k < n_units && !stop) {
@@ -448,7 +448,6 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       }
     }
   }
-  pdl_wait();  // the codebook table needs only the codebooks; the rest waits for the previous kernel
   int len_r = 0;
   if (tid < n_units) len_r = __ldg(p.seq_lens + unit_id(p, tid).b);
   uint2 q_r = make_uint2(0, 0);
@@ -743,6 +742,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       m_run[gi] = -INFINITY;
       l_run[gi] = 0.f;
     }
+    if (k == 0) pdl_wait();  // partials are written only after the previous kernel completes
 #pragma unroll
     for (int nn = 0; nn < kNCH; ++nn) {  // nothing pending yet
       pb[nn][0][0] = pb[nn][0][1] = pb[nn][1][0] = pb[nn][1][1] = 0u;

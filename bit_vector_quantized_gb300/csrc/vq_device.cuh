@@ -28,11 +28,12 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 // ------------------------------------------- programmatic dependent launch ---
 // The library's kernels are launched with programmatic stream serialization:
 // a kernel may be scheduled while the previous kernel in the stream still runs
-// if that kernel signals pdl_trigger (only the library's own kernels do).
-// Before pdl_wait a kernel reads nothing but the codebooks, which none of the
-// library's kernels writes; pdl_wait blocks until the previous kernel has
-// completed and its memory is visible.  Without the launch attribute both are
-// no-ops.
+// if that kernel signals pdl_trigger, which only the library's own kernels do.
+// Those write nothing but code pools, workspaces, outputs and status words, so
+// before pdl_wait a kernel reads only inputs that are none of these
+// (codebooks, lambda, queries, new keys/values, page tables, lengths, slots)
+// and writes nothing; pdl_wait blocks until the previous kernel has completed
+// and its memory is visible.  Without the launch attribute both are no-ops.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -146,6 +146,7 @@ __device__ __forceinline__ void pack_store(const EncodeParams& p, int which, con
   const int bits = p.bits[which];
   const int S = kHeadDim / D;
   const int row_words = p.row_bytes[which] / 4;
+  pdl_wait();  // the pool may be read by the previous kernel: store only after it
   const int i_lo = (32 * lane) / bits;
   const int kmax = 32 / bits + 2;
   uint32_t word = 0;
@@ -364,7 +365,6 @@ __global__ void __launch_bounds__(kEncWarps * 32) vq_encode_kernel(const EncodeP
     }
     cnorm[j] = n;
   }
-  pdl_wait();  // the codebook table needs only the codebook; the rest waits for the previous kernel
   if (p.vec_per_warp == kMultiVec) {  // prefill: several vectors per warp (sub-vector length 2 or 4)
     if (d == 4) encode_multi<4, kMultiVec>(p, which, cmul, cnorm);
     else encode_multi<2, kMultiVec>(p, which, cmul, cnorm);

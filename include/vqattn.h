@@ -18,6 +18,13 @@
  *   - Every call is asynchronous and ordered on the CUDA stream `stream`
  *     (a cudaStream_t passed as void*; NULL = the legacy default stream).
  *     No call synchronises the device.
+ *   - Kernels are launched with programmatic stream serialization.  When the
+ *     previous kernel in the stream is one of this library's, a kernel may
+ *     start before it has finished and read its inputs that are not pools,
+ *     workspaces, outputs or status words (codebooks, lambda, queries, new
+ *     keys/values, page tables, lengths, slots); it reads no pool and writes
+ *     nothing until that kernel has completed.  Those inputs must therefore
+ *     not alias a pool, workspace, output or status word of an earlier call.
  *   - Arguments are validated on the host before anything is launched; a
  *     failed check returns a negative vq_status and launches nothing.
  *     vq_last_error() then describes the failure (thread-local string).
