@@ -65,6 +65,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--soak-seconds", type=float, default=1.5)
+    ap.add_argument("--no-fp16-compare", action="store_true",
+                    help="skip the dense fp16 attention comparison (context only)")
     return ap.parse_args()
 
 
@@ -246,6 +248,53 @@ def run_reference(args, w, rank):
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def fp16_comparison(torch, w, dev, steps, l2):
+    """Context, not the product path: PyTorch's scaled_dot_product_attention
+    (a library kernel) for one decode query per sequence over dense fp16 K/V of
+    the same shape (every sequence padded to the longest; GQA), timed like the
+    step: a CUDA graph of `steps` launches over rotating copies larger than L2."""
+    import torch.nn.functional as F
+    B, Hq, Hkv, D = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+    N = int(W.seq_lens(w).max()) + 1
+    kv_bytes = 2 * B * Hkv * N * D * 2
+    copies = max(1, -(-2 * l2 // kv_bytes))
+    if kv_bytes * copies > 24e9:
+        return {"skipped": "dense fp16 K/V would not fit the memory budget"}
+    g = torch.Generator(device=dev).manual_seed(0)
+    q = torch.randn((B, Hq, 1, D), generator=g, device=dev, dtype=torch.float16)
+    kvs = [(torch.randn((B, Hkv, N, D), generator=g, device=dev, dtype=torch.float16),
+            torch.randn((B, Hkv, N, D), generator=g, device=dev, dtype=torch.float16)) for _ in range(copies)]
+
+    def one(i):
+        k, v = kvs[i % copies]
+        return F.scaled_dot_product_attention(q, k, v, enable_gqa=True)
+
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(gr, stream=s):
+            for i in range(steps):
+                one(i)
+    torch.cuda.current_stream().wait_stream(s)
+    gr.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    gr.replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    del kvs
+    torch.cuda.empty_cache()
+    return {"kernel": "torch scaled_dot_product_attention, fp16 K/V, enable_gqa", "us_per_step": ms * 1e3,
+            "kv_bytes_per_step": kv_bytes, "hbm_gbs": kv_bytes / (ms / 1e3) / 1e9,
+            "padded_tokens_per_sequence": N}
 
 
 def encode_report(w, tokens, ms, sms, clocks):
@@ -518,6 +567,16 @@ def main():
                "h2d_bytes_per_step": q_p.numel() * 2 + k_p.numel() * 2 + v_p.numel() * 2,
                "d2h_bytes_per_step": out_p.numel() * 2, "ms_per_step": e_ms}
 
+    comparison = None
+    if world == 1 and not args.no_fp16_compare:
+        try:
+            comparison = fp16_comparison(torch, w, dev, min(K, 200), l2)
+            if "us_per_step" in comparison:
+                comparison["step_speedup_vs_fp16"] = comparison["us_per_step"] / (1e3 * ms_per_step)
+                comparison["attention_speedup_vs_fp16"] = comparison["us_per_step"] / (1e3 * split_launch_ms)
+        except Exception as exc:  # context only: never fail the bench line on it
+            comparison = {"skipped": f"{type(exc).__name__}: {exc}"[:200]}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = run_cpu_baseline(w, lam, ck, cv, args.cpu_seconds)
@@ -543,6 +602,7 @@ def main():
                              "split_attention_back_to_back": 1e3 * split_launch_ms,
                              "combine": 1e3 * float(np.mean(comb_ms)), "step": 1e3 * ms_per_step},
             "prefill_encode": encode_report(w, prefill_tokens, enc_ms, sms, clocks),
+            "fp16_comparison": comparison,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * K, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
