@@ -412,6 +412,20 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       else cbv_r[i].x = __ldg(reinterpret_cast<const uint32_t*>(p.cb_v) + j);
     }
   }
+  int len_r = 0;
+  if (tid < n_units) len_r = __ldg(p.seq_lens + unit_id(p, tid).b);
+  uint2 q_r = make_uint2(0, 0);
+  float4 lam_r = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto load_q = [&](int k) {  // query and lambda of unit k (consumer warps < G)
+    if (warp < G && k < n_units) {
+      const UnitId id = unit_id(p, k);
+      q_r = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.q) +
+                                               (static_cast<long long>(id.b) * p.hq + id.kvh * G + warp) * kHeadDim) +
+                  lane);
+      lam_r = __ldg(reinterpret_cast<const float4*>(p.lambda + id.kvh * kHeadDim) + lane);
+    }
+  };
+  load_q(0);
   {  // codebook table: row j = 16 copies of 8-byte (32 copies of 4-byte) K centroid j,
      // then the same for V centroid j
     const uint32_t tab = smem_addr(smem + L.tab);
@@ -448,20 +462,6 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       }
     }
   }
-  int len_r = 0;
-  if (tid < n_units) len_r = __ldg(p.seq_lens + unit_id(p, tid).b);
-  uint2 q_r = make_uint2(0, 0);
-  float4 lam_r = make_float4(0.f, 0.f, 0.f, 0.f);
-  auto load_q = [&](int k) {  // query and lambda of unit k (consumer warps < G)
-    if (warp < G && k < n_units) {
-      const UnitId id = unit_id(p, k);
-      q_r = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.q) +
-                                               (static_cast<long long>(id.b) * p.hq + id.kvh * G + warp) * kHeadDim) +
-                  lane);
-      lam_r = __ldg(reinterpret_cast<const float4*>(p.lambda + id.kvh * kHeadDim) + lane);
-    }
-  };
-  load_q(0);
   if (tid < n_units) ulen_c[tid] = clamp_len(len_r);
   consumer_sync<NW>();  // codebooks and unit lengths visible to the consumers
 
@@ -834,26 +834,42 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
 }
 
 // Merge of the split partials: o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
+// Each thread (one output element) loads all of its (m, l) pairs and partial
+// outputs of a chunk of up to 32 splits before using any (one round trip to
+// L2, bypassing L1: the partials were written by the previous kernel), then
+// merges them; chunks after the first rescale the running sums.  With at most
+// kC splits the sums are formed in split order from the global maximum.
+template <int kC>
 __global__ void __launch_bounds__(kHeadDim) vq_combine_kernel(const CombineParams p) {
-  extern __shared__ float2 cml[];  // [splits]
   const int row = blockIdx.x, d = threadIdx.x;
   pdl_trigger();
   pdl_wait();
   const float2* ml = p.ws_ml + static_cast<long long>(row) * p.splits;
   const float* o = p.ws_o + static_cast<long long>(row) * p.splits * kHeadDim + d;
-  for (int s = d; s < p.splits; s += kHeadDim) cml[s] = ml[s];
-  __syncthreads();
-  float M = -INFINITY;
-  for (int s = 0; s < p.splits; ++s) M = fmaxf(M, cml[s].x);
-  float acc = 0.f, l = 0.f;
-  if (M != -INFINITY) {
-#pragma unroll 16
-    for (int s = 0; s < p.splits; ++s) {
-      const float2 v = cml[s];
-      const float f = fast_exp2(v.x - M);
-      acc = fmaf(f, __ldg(o + s * kHeadDim), acc);
-      l = fmaf(f, v.y, l);
+  float M = -INFINITY, acc = 0.f, l = 0.f;
+  for (int s0 = 0; s0 < p.splits; s0 += kC) {
+    float2 v[kC];
+    float ov[kC];
+#pragma unroll
+    for (int i = 0; i < kC; ++i) {
+      const int sp = s0 + i;
+      v[i] = sp < p.splits ? __ldcg(ml + sp) : make_float2(-INFINITY, 0.f);
+      ov[i] = sp < p.splits ? __ldcg(o + static_cast<long long>(sp) * kHeadDim) : 0.f;
     }
+    float Mc = M;
+#pragma unroll
+    for (int i = 0; i < kC; ++i) Mc = fmaxf(Mc, v[i].x);
+    if (Mc == -INFINITY) continue;
+    const float a = fast_exp2(M - Mc);  // 0 while nothing is accumulated yet
+    acc *= a;
+    l *= a;
+#pragma unroll
+    for (int i = 0; i < kC; ++i) {
+      const float f = fast_exp2(v[i].x - Mc);
+      acc = fmaf(f, ov[i], acc);
+      l = fmaf(f, v[i].y, l);
+    }
+    M = Mc;
   }
   const float res = l > 0.f ? acc / l : 0.f;
   static_cast<__half*>(p.out)[static_cast<long long>(row) * kHeadDim + d] = __float2half_rn(res);
@@ -914,14 +930,10 @@ cudaError_t launch_decode(const DecodeParams& p, int k_sub, int k_bits, int v_su
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
   if (p.rows == 0) return cudaSuccess;
-  static bool configured = false;
-  const size_t smem = static_cast<size_t>(p.splits) * sizeof(float2);
-  if (!configured) {
-    cudaError_t e = configure(vq_combine_kernel, 48 * 1024);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  cudaError_t e = launch_pdl(vq_combine_kernel, dim3(p.rows), dim3(kHeadDim), smem, stream, p);
+  // chunk of splits loaded at once: the smallest of 4, 8, 16, 32 that holds them all
+  auto kern = p.splits <= 4 ? vq_combine_kernel<4> : p.splits <= 8 ? vq_combine_kernel<8>
+            : p.splits <= 16 ? vq_combine_kernel<16> : vq_combine_kernel<32>;
+  cudaError_t e = launch_pdl(kern, dim3(p.rows), dim3(kHeadDim), 0, stream, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

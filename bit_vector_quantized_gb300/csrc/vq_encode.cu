@@ -355,6 +355,9 @@ __global__ void __launch_bounds__(kEncWarps * 32) vq_encode_kernel(const EncodeP
   float* red_best = cnorm + ((ncent + 3) & ~3);
   int* red_idx = reinterpret_cast<int*>(red_best + kEncWarps * 32 * 4);
   pdl_trigger();
+  // the vector's loads go out first, so they overlap the codebook loads below
+  VecIn in{};
+  if (p.vec_per_warp != kMultiVec) in = load_vector(p, which);
   const __half* cb = static_cast<const __half*>(p.cb[which]);
   for (int j = threadIdx.x; j < ncent; j += blockDim.x) {
     float n = 0.f;
@@ -370,7 +373,6 @@ __global__ void __launch_bounds__(kEncWarps * 32) vq_encode_kernel(const EncodeP
     else encode_multi<2, kMultiVec>(p, which, cmul, cnorm);
     return;
   }
-  const VecIn in = load_vector(p, which);
   __syncthreads();
   switch (d) {
     case 1: encode_vector<1>(p, which, in, cmul, cnorm, red_best, red_idx); break;
