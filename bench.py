@@ -4,11 +4,12 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload I]
 
-One step = the whole decode hot path for one batch: encode the appended token
-of every sequence (vq_encode_kv), split attention over the quantized cache
-(vq_decode_partial) and the split combine (vq_decode_combine).  The default
-workload is Llama-3.1-8B layer shape, batch 1, 32 query / 8 KV heads, 32768
-cached tokens (+1 appended), 2-bit K and V codes (d = 4, 256 centroids).
+One step = the whole decode hot path for one batch, one vq_decode_step call:
+encode the appended token of every sequence into the cache (slots from the
+page table), split attention over the quantized cache and the split combine.
+The default workload is Llama-3.1-8B layer shape, batch 1, 32 query / 8 KV
+heads, 32768 cached tokens (+1 appended), 2-bit K and V codes (d = 4, 256
+centroids).
 
 Timing: W eager warm-up steps; then exactly K steps captured in one CUDA graph
 and replayed between CUDA events, with a barrier and a synchronize on both
@@ -429,7 +430,17 @@ def main():
     def p(t):
         return t.data_ptr()
 
-    def step(i, ev=None):
+    def step(i):
+        """The hot path: vq_decode_step (append, split attention, merge)."""
+        kp, vp = pools[i % copies]
+        vq.vq_decode_step(layout, B, p(q_d), p(k_new), p(v_new), p(lam_d), p(ck_d), p(cv_d),
+                          p(kp), p(vp), num_pages, p(table_d), table_d.shape[1], p(seq_d), max_len,
+                          0.0, splits, p(out), p(ws), ws_bytes, p(status),
+                          torch.cuda.current_stream().cuda_stream)
+
+    def step_unfused(i, ev=None):
+        """The same step through the separate calls (vq_encode_kv, vq_decode_partial,
+        vq_decode_combine), with optional events around each kernel."""
         kp, vp = pools[i % copies]
         stream = torch.cuda.current_stream().cuda_stream
         if ev is not None:
@@ -483,7 +494,7 @@ def main():
     try:
         evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
                for _ in range(n_ev)]
-        g_ev = capture(lambda i: step(i, evs[i]), n_ev)
+        g_ev = capture(lambda i: step_unfused(i, evs[i]), n_ev)
         graph_events = True
     except (TypeError, RuntimeError):
         evs, g_ev, graph_events = None, None, False
@@ -517,7 +528,7 @@ def main():
     else:  # eager fallback: events around each launch after the timed region
         ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(min(K, 500))]
         for i, e in enumerate(ev2):
-            step(i, e)
+            step_unfused(i, e)
         torch.cuda.synchronize()
         split_ms = [e[1].elapsed_time(e[2]) for e in ev2]
         append_ms = [e[0].elapsed_time(e[1]) for e in ev2]

@@ -138,6 +138,44 @@ vq_status vq_check_layout(const vq_layout* layout, int32_t for_decode) {
   return check_layout_impl(layout, for_decode);
 }
 
+// Launches the encode of num_tokens tokens: the caller has set the sources,
+// codebooks, pools, lambda, the slot source and the status word; the launch
+// shape follows from the number of vectors.
+vq_status launch_encode_impl(const vq_layout& L, vqk::EncodeParams& p, int32_t num_tokens,
+                             bool has_k, bool has_v, void* stream, const char* what) {
+  p.sub[0] = L.k_sub;
+  p.sub[1] = L.v_sub;
+  p.bits[0] = L.k_bits;
+  p.bits[1] = L.v_bits;
+  p.row_bytes[0] = static_cast<int>(vq_code_row_bytes(L.head_dim, L.k_sub, L.k_bits));
+  p.row_bytes[1] = static_cast<int>(vq_code_row_bytes(L.head_dim, L.v_sub, L.v_bits));
+  p.num_tokens = num_tokens;
+  p.hkv = L.num_kv_heads;
+  p.page_size = L.page_size;
+  const long long vectors = static_cast<long long>(num_tokens) * L.num_kv_heads;
+  const int sms = device_sms();
+  // few vectors (a decode-step append): spread each codebook scan over 8 warps
+  p.split = vectors * 2 < static_cast<long long>(sms > 0 ? sms : 148) * 8 ? 8 : 1;
+  // many vectors with sub-vector lengths 2 / 4: several vectors per warp
+  const bool multi_ok = (!has_k || L.k_sub == 2 || L.k_sub == 4) && (!has_v || L.v_sub == 2 || L.v_sub == 4);
+  p.vec_per_warp = (p.split == 1 && multi_ok) ? vqk::kMultiVec : 1;
+  const int per_cta = 8 * p.vec_per_warp / p.split;
+  const long long grid_x = (vectors + per_cta - 1) / per_cta;
+  if (grid_x > 0x7fffffffLL) return fail(VQ_ERR_INVALID_ARG, "too many tokens (%d)", num_tokens);
+  p.which_base = has_k ? 0 : 1;
+  const int grid_y = (has_k && has_v) ? 2 : 1;
+  size_t smem = 0;
+  if (has_k) smem = std::max(smem, vqk::encode_smem_bytes(L.k_sub, L.k_bits));
+  if (has_v) smem = std::max(smem, vqk::encode_smem_bytes(L.v_sub, L.v_bits));
+  const int optin = device_smem_optin();
+  if (optin > 0 && smem > static_cast<size_t>(optin))
+    return fail(VQ_ERR_UNSUPPORTED, "encode needs %zu bytes of shared memory, device has %d", smem, optin);
+  cudaError_t e = vqk::launch_encode(p, static_cast<int>(grid_x), grid_y, smem,
+                                     static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return VQ_OK;
+}
+
 vq_status vq_encode_kv(const vq_layout* layout, int32_t num_tokens, const void* k, const void* v,
                        const int64_t* slot_mapping, const float* lambda, const void* codebook_k,
                        const void* codebook_v, void* k_pool, void* v_pool, int64_t num_pages,
@@ -165,41 +203,12 @@ vq_status vq_encode_kv(const vq_layout* layout, int32_t num_tokens, const void* 
   p.cb[1] = codebook_v;
   p.pool[0] = static_cast<uint8_t*>(k_pool);
   p.pool[1] = static_cast<uint8_t*>(v_pool);
-  p.sub[0] = L.k_sub;
-  p.sub[1] = L.v_sub;
-  p.bits[0] = L.k_bits;
-  p.bits[1] = L.v_bits;
-  p.row_bytes[0] = static_cast<int>(vq_code_row_bytes(L.head_dim, L.k_sub, L.k_bits));
-  p.row_bytes[1] = static_cast<int>(vq_code_row_bytes(L.head_dim, L.v_sub, L.v_bits));
   p.lambda = lambda;
   p.slots = slot_mapping;
   p.status = status;
   p.num_slots = static_cast<long long>(num_pages) * L.page_size;
-  p.num_tokens = num_tokens;
-  p.hkv = L.num_kv_heads;
-  p.page_size = L.page_size;
-  const long long vectors = static_cast<long long>(num_tokens) * L.num_kv_heads;
-  const int sms = device_sms();
-  // few vectors (a decode-step append): spread each codebook scan over 8 warps
-  p.split = vectors * 2 < static_cast<long long>(sms > 0 ? sms : 148) * 8 ? 8 : 1;
-  // many vectors with sub-vector lengths 2 / 4: several vectors per warp
-  const bool multi_ok = (!k || L.k_sub == 2 || L.k_sub == 4) && (!v || L.v_sub == 2 || L.v_sub == 4);
-  p.vec_per_warp = (p.split == 1 && multi_ok) ? vqk::kMultiVec : 1;
-  const int per_cta = 8 * p.vec_per_warp / p.split;
-  const long long grid_x = (vectors + per_cta - 1) / per_cta;
-  if (grid_x > 0x7fffffffLL) return fail(VQ_ERR_INVALID_ARG, "too many tokens (%d)", num_tokens);
-  p.which_base = k ? 0 : 1;
-  const int grid_y = (k && v) ? 2 : 1;
-  size_t smem = 0;
-  if (k) smem = std::max(smem, vqk::encode_smem_bytes(L.k_sub, L.k_bits));
-  if (v) smem = std::max(smem, vqk::encode_smem_bytes(L.v_sub, L.v_bits));
-  const int optin = device_smem_optin();
-  if (optin > 0 && smem > static_cast<size_t>(optin))
-    return fail(VQ_ERR_UNSUPPORTED, "encode needs %zu bytes of shared memory, device has %d", smem, optin);
-  cudaError_t e = vqk::launch_encode(p, static_cast<int>(grid_x), grid_y, smem,
-                                     static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "vq_encode_kv launch");
-  return VQ_OK;
+  return launch_encode_impl(L, p, num_tokens, k != nullptr, v != nullptr, stream,
+                            "vq_encode_kv launch");
 }
 
 int32_t vq_default_num_splits(const vq_layout* layout, int32_t batch, int32_t max_seq_len,
@@ -334,6 +343,8 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
   return VQ_OK;
 }
 
+// CTAs of the decode step's append encode: one warp per (sequence, KV head)
+// vector, 8 per CTA, keys and values.
 vq_status launch_partial(const vq_layout& L, const vqk::DecodeParams& p, int grid, size_t smem,
                          void* stream) {
   cudaError_t e = vqk::launch_decode(p, L.k_sub, L.k_bits, L.v_sub, L.v_bits, grid, smem,
@@ -404,6 +415,55 @@ vq_status vq_decode_combine(const vq_layout* layout, int32_t batch, int32_t max_
   if (batch < 0 || max_seq_len < 0) return fail(VQ_ERR_INVALID_ARG, "batch or max_seq_len < 0");
   if (batch == 0) return VQ_OK;
   return combine_impl(layout, batch, max_seq_len, num_splits, workspace, workspace_bytes, out, stream);
+}
+
+vq_status vq_decode_step(const vq_layout* layout, int32_t batch, const void* q, const void* k_new,
+                         const void* v_new, const float* lambda, const void* codebook_k,
+                         const void* codebook_v, void* k_pool, void* v_pool, int64_t num_pages,
+                         const int32_t* page_table, int32_t max_pages_per_seq,
+                         const int32_t* seq_lens, int32_t max_seq_len, float softmax_scale,
+                         int32_t num_splits, void* out, void* workspace, size_t workspace_bytes,
+                         int32_t* status, void* stream) {
+  vq_status st = check_layout_impl(layout, 1);
+  if (st != VQ_OK) return st;
+  const vq_layout& L = *layout;
+  if (batch < 0) return fail(VQ_ERR_INVALID_ARG, "batch %d < 0", batch);
+  if (batch == 0) return VQ_OK;
+  const void* ptrs[] = {k_new, v_new, out};
+  const char* names[] = {"k_new", "v_new", "out"};
+  for (int i = 0; i < 3; ++i) {
+    if (!ptrs[i]) return fail(VQ_ERR_INVALID_ARG, "%s is NULL", names[i]);
+    if (!aligned16(ptrs[i])) return fail(VQ_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+  }
+  vqk::DecodeParams p;
+  int grid = 0;
+  size_t smem = 0;
+  st = prepare_decode(layout, batch, q, lambda, codebook_k, codebook_v, k_pool, v_pool, num_pages,
+                      page_table, max_pages_per_seq, seq_lens, max_seq_len, softmax_scale,
+                      num_splits, workspace, workspace_bytes, status, p, grid, smem);
+  if (st != VQ_OK) return st;
+
+  // 1. append: token seq_lens[b] - 1 of every sequence, slot from the page table
+  vqk::EncodeParams ep{};
+  ep.src[0] = k_new;
+  ep.src[1] = v_new;
+  ep.cb[0] = codebook_k;
+  ep.cb[1] = codebook_v;
+  ep.pool[0] = static_cast<uint8_t*>(k_pool);
+  ep.pool[1] = static_cast<uint8_t*>(v_pool);
+  ep.lambda = lambda;
+  ep.slots = nullptr;
+  ep.page_table = page_table;
+  ep.seq_lens = seq_lens;
+  ep.max_pages = max_pages_per_seq;
+  ep.status = status;
+  ep.num_slots = static_cast<long long>(num_pages) * L.page_size;
+  st = launch_encode_impl(L, ep, batch, true, true, stream, "vq_decode_step append encode");
+  if (st != VQ_OK) return st;
+  // 2. split attention (its copies wait for the append), 3. merge of the splits
+  st = launch_partial(L, p, grid, smem, stream);
+  if (st != VQ_OK) return st;
+  return combine_impl(layout, batch, max_seq_len, p.splits, workspace, workspace_bytes, out, stream);
 }
 
 vq_status vq_decode_attention(const vq_layout* layout, int32_t batch, const void* q,

@@ -102,6 +102,19 @@ __device__ __forceinline__ void scan_centroids(const float (&x)[4], const float*
   }
 }
 
+// Slot of token t: from slot_mapping, or (decode-step append, no slot mapping)
+// position seq_lens[t] - 1 of sequence t through its page table.  -1: nothing to
+// store (padding, or an empty sequence); -2: the page-table entry is invalid.
+__device__ __forceinline__ long long token_slot(const EncodeParams& p, long long t) {
+  if (p.slots) return __ldg(p.slots + t);
+  const int len = __ldg(p.seq_lens + t);
+  if (len <= 0) return -1;
+  const int pos = len - 1, pi = pos / p.page_size;
+  const int page = pi < p.max_pages ? __ldg(p.page_table + t * p.max_pages + pi) : -1;
+  if (page < 0 || static_cast<long long>(page) * p.page_size >= p.num_slots) return -2;
+  return static_cast<long long>(page) * p.page_size + pos % p.page_size;
+}
+
 // One warp's vector: its location and the values loaded before the codebook
 // barrier, so that every global load of the CTA is in flight at once.
 struct VecIn {
@@ -129,7 +142,7 @@ __device__ __forceinline__ VecIn load_vector(const EncodeParams& p, int which) {
                                                   (in.t * p.hkv + in.h) * kHeadDim) +
                    lane);
     if (which == 0) in.lam = __ldg(reinterpret_cast<const float4*>(p.lambda + in.h * kHeadDim) + lane);
-    in.slot = __ldg(p.slots + in.t);
+    in.slot = token_slot(p, in.t);
   }
   return in;
 }
@@ -174,6 +187,10 @@ __device__ __forceinline__ void pack_store(const EncodeParams& p, int which, con
     }
   }
   if (!active || lane >= row_words) return;
+  if (slot == -2) {  // the appended token's page is out of range
+    if (lane == 0) report(p.status, kDevBadPage);
+    return;
+  }
   if (slot < 0) return;  // padding token
   if (slot >= p.num_slots) {
     if (lane == 0) report(p.status, kDevBadSlot);
@@ -275,7 +292,7 @@ __device__ void encode_multi(const EncodeParams& p, int which, const float* cmul
       raw[v] = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.src[which]) +
                                                     (t * p.hkv + hh[v]) * kHeadDim) + lane);
       if (which == 0) lam[v] = __ldg(reinterpret_cast<const float4*>(p.lambda + hh[v] * kHeadDim) + lane);
-      slot[v] = __ldg(p.slots + t);
+      slot[v] = token_slot(p, t);
     }
   }
   __syncthreads();  // the codebook table is ready

@@ -24,6 +24,11 @@ struct EncodeParams {
   int split;             // warps per token-head: 1, 2, 4 or 8
   int which_base;        // blockIdx.y + which_base selects keys (0) or values (1)
   int vec_per_warp;      // 1, or kMultiVec (prefill with sub-vector lengths 2 / 4; split == 1)
+  // Decode-step append (slots == NULL): token t is the new token of sequence t,
+  // stored at position seq_lens[t] - 1 through the page table.
+  const int32_t* page_table;  // [T][max_pages]
+  const int32_t* seq_lens;    // [T]
+  int max_pages;
 };
 
 constexpr int kMultiVec = 4;  // vectors per warp of the prefill encode

@@ -214,6 +214,39 @@ vq_status vq_decode_combine(const vq_layout* layout, int32_t batch, int32_t max_
                             void* out, void* stream);
 
 /*
+ * One decode step: append each sequence's new token to the cache, then decode
+ * attention over the cache with the new token included (VecInfer, section
+ * 方法细节 "注意力机制中的向量量化KV缓存": during decoding the new key and value
+ * are encoded and appended, then the query attends over the quantized cache).
+ * Exactly the results of vq_encode_kv of the new tokens followed by
+ * vq_decode_attention with the same split count, without a slot mapping: the
+ * slots come from the page table.  Three kernels on `stream` (append encode,
+ * split attention, merge); the attention kernel starts while the append is
+ * encoding, prepares its codebook tables, and waits for the append before it
+ * reads the pools.
+ *   k_new, v_new fp16 [batch][Hkv][D]: the new token of every sequence.  It is
+ *                token seq_lens[b] - 1 of sequence b and goes to slot
+ *                page_table[b][t / P] * P + t % P of the pools
+ *                (t = seq_lens[b] - 1).  seq_lens[b] == 0 appends nothing and
+ *                gives a zero output row.  An out-of-range page for the new
+ *                token reports VQ_DEV_BAD_PAGE; it is neither stored nor
+ *                attended.
+ *   k_pool, v_pool are written (the new rows) as well as read.
+ *   workspace    at least vq_decode_workspace_bytes(layout, batch,
+ *                max_seq_len, num_splits, 0) bytes, 256-byte aligned; no
+ *                initialisation needed.
+ * All other arguments, the split choice for num_splits <= 0 and the errors are
+ * those of vq_decode_attention.
+ */
+vq_status vq_decode_step(const vq_layout* layout, int32_t batch, const void* q, const void* k_new,
+                         const void* v_new, const float* lambda, const void* codebook_k,
+                         const void* codebook_v, void* k_pool, void* v_pool, int64_t num_pages,
+                         const int32_t* page_table, int32_t max_pages_per_seq,
+                         const int32_t* seq_lens, int32_t max_seq_len, float softmax_scale,
+                         int32_t num_splits, void* out, void* workspace, size_t workspace_bytes,
+                         int32_t* status, void* stream);
+
+/*
  * Decode attention for callers that cannot allocate device memory.
  *
  * No counterpart on the VecInfer pages: this is a deployment variant of

@@ -205,6 +205,25 @@ class GpuCache:
         t.cuda.synchronize()
         return out.float().cpu().numpy()
 
+    def step(self, q: Optional[np.ndarray] = None, lens: Optional[np.ndarray] = None,
+             num_splits: int = 0) -> np.ndarray:
+        """Decode step through vq_decode_step: appends token lens_b - 1 of every
+        sequence (default lens: N_b + 1, i.e. token N_b) and attends over lens_b tokens."""
+        t = self.torch
+        q = W.queries(self.w) if q is None else q
+        lens = self.lens + 1 if lens is None else lens
+        pos = [max(int(n) - 1, 0) for n in lens]
+        k = np.stack([W.kv_tokens(self.w, b, "k", p, p + 1)[0] for b, p in enumerate(pos)])
+        v = np.stack([W.kv_tokens(self.w, b, "v", p, p + 1)[0] for b, p in enumerate(pos)])
+        seq = t.from_numpy(lens.astype(np.int32)).to(self.device)
+        out = self.vq.decode_step(self.layout, t.from_numpy(q).to(self.device),
+                                  t.from_numpy(k).to(self.device), t.from_numpy(v).to(self.device),
+                                  self.lam, self.ck, self.cv, self.k_pool, self.v_pool,
+                                  self.page_table, seq, int(lens.max()) if len(lens) else 0,
+                                  num_splits=num_splits, status=self.status)
+        t.cuda.synchronize()
+        return out.float().cpu().numpy()
+
     def device_status(self) -> int:
         self.torch.cuda.synchronize()
         return int(self.status.item())
