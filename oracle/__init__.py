@@ -48,6 +48,8 @@ def lib():
             "vqo_kmeans": (None, [L, I, I, P, P, I, P, P]),
             "vqo_pack": (I, [L, I, I, P, I, P]),
             "vqo_unpack": (None, [L, I, I, P, I, P]),
+            "vqo_dequantize": (None, [L, I, I, P, P, P]),
+            "vqo_inverse_transform_keys": (None, [L, I, I, P, P, P, P]),
             "vqo_decode_attention": (None, [L, I, I, I, P, P, P, I, P, P, I, P, P, D, P]),
             "vqo_attention_fp": (None, [L, I, I, I, P, P, P, D, P]),
         }
@@ -183,6 +185,34 @@ def encode_values(v: np.ndarray, Cv: np.ndarray, d: int):
     codes, best, second, _ = vq_assign(x.reshape(-1, d), Cv)
     shp = (T, Hkv, D // d)
     return codes.reshape(shp), x, best.reshape(shp), second.reshape(shp)
+
+
+def dequantize(codes: np.ndarray, C: np.ndarray) -> np.ndarray:
+    """fp64 [..][S * d]: the centroids named by codes [..][S], concatenated."""
+    codes = np.ascontiguousarray(codes, dtype=np.int32)
+    C = _f64(C)
+    S, d = codes.shape[-1], C.shape[1]
+    n = codes.size // S if S else 0
+    out = np.zeros(codes.shape[:-1] + (S * d,))
+    lib().vqo_dequantize(n, S, d, _p(codes), _p(C), _p(out))
+    return out
+
+
+def inverse_transform_keys(kt: np.ndarray, lam: np.ndarray) -> np.ndarray:
+    """fp64 K = K~ H diag(lam) for transformed keys [T][Hkv][D]."""
+    kt = _f64(kt)
+    T, Hkv, D = kt.shape
+    lam, H = _f64(lam), hadamard(D)
+    out = np.zeros_like(kt)
+    lib().vqo_inverse_transform_keys(T, Hkv, D, _p(kt), _p(lam), _p(H), _p(out))
+    return out
+
+
+def dequantize_kv(k_codes: np.ndarray, Ck: np.ndarray, v_codes: np.ndarray, Cv: np.ndarray,
+                  lam: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """fp64 (K^, V^) [T][Hkv][D] in the original key and value spaces from codes
+    [T][Hkv][S]: K^ = VQ^-1(K~_q) H diag(lam), V^ = VQ^-1(V_q)."""
+    return inverse_transform_keys(dequantize(k_codes, Ck), lam), dequantize(v_codes, Cv)
 
 
 def decode_attention(q: np.ndarray, lam: np.ndarray, k_codes: np.ndarray, Ck: np.ndarray,

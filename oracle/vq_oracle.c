@@ -250,6 +250,41 @@ void vqo_unpack(long n, int S, int b, const uint8_t *in, int row_bytes, int32_t 
 }
 
 /*
+ * Dequantisation VQ^-1 (VecInfer, 背景知识 "向量量化原理" and 方法细节 /
+ * "注意力机制中的向量量化KV缓存"): a vector is stored as the indices of its
+ * sub-vectors' nearest centroids, and read back as the concatenation of those
+ * centroids.  codes: [n][S]; C: [2^b][d]; out: [n][S * d].
+ */
+void vqo_dequantize(long n, int S, int d, const int32_t *codes, const double *C, double *out) {
+  for (long v = 0; v < n; ++v)
+    for (int i = 0; i < S; ++i) {
+      const double *c = C + (long)codes[v * S + i] * d;
+      for (int e = 0; e < d; ++e) out[(v * S + i) * d + e] = c[e];
+    }
+}
+
+/*
+ * Inverse of the key transform (VecInfer, 方法细节 / "Hadamard引理与注意力分数重写"
+ * defines K~ = K diag(lambda)^-1 H_D).  H_D is symmetric and orthonormal
+ * (H_D H_D = I), so K = K~ H_D diag(lambda): a dense row-vector times matrix
+ * product, then a per-channel multiply.  Kt, K: [T][Hkv][D]; lam: [Hkv][D].
+ */
+void vqo_inverse_transform_keys(long T, int Hkv, int D, const double *Kt, const double *lam,
+                                const double *H, double *K) {
+#pragma omp parallel for schedule(static)
+  for (long th = 0; th < T * Hkv; ++th) {
+    const int h = (int)(th % Hkv);
+    const double *x = Kt + th * D;
+    double *o = K + th * D;
+    for (int j = 0; j < D; ++j) {
+      double s = 0.0;
+      for (int l = 0; l < D; ++l) s += x[l] * H[(long)l * D + j];
+      o[j] = s * lam[h * D + j];
+    }
+  }
+}
+
+/*
  * Decode attention over vector-quantized caches for one sequence (VecInfer,
  * 方法细节 / "注意力机制中的向量量化KV缓存"):
  *   s = q~ VQ^-1(K~_q, C_k)^T * scale,  p = softmax(s),  o = p VQ^-1(V_q, C_v)

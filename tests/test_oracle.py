@@ -278,6 +278,55 @@ def test_exact_codebook_encode_and_attention(dk, dv):
     assert np.max(np.abs(out_q - out_fp)) < 1e-12
 
 
+# ---------------------------------------------------------- dequantisation ---
+
+def test_dequantize_golden_d2():
+    f = _fixture("dequant_d2.txt")
+    Ck = np.array(f["ck"][0]).reshape(2, 2)
+    Cv = np.array(f["cv"][0]).reshape(2, 2)
+    kc = np.array(f["kcode"][0], np.int32).reshape(1, 1, 1)
+    vc = np.array(f["vcode"][0], np.int32).reshape(1, 1, 1)
+    lam = np.array(f["lambda"][0]).reshape(1, 2)
+    k, v = oracle.dequantize_kv(kc, Ck, vc, Cv, lam)
+    assert np.max(np.abs(k[0, 0] - np.array(f["k"][0]))) < 1e-15
+    assert np.array_equal(v[0, 0], np.array(f["v"][0]))
+
+
+@pytest.mark.parametrize("dk,dv", [(2, 4), (4, 4), (1, 2), (8, 8)])
+def test_dequantize_kv_recovers_codebook_built_cache(dk, dv):
+    """Caches built from codebook rows with scipy's Hadamard come back exactly."""
+    rng = np.random.default_rng(40 + dk)
+    _, k, v, lam, Ck, Cv, kc, vc = _exact_codebook_case(rng, 29, 4, 3, 128, dk, dv, 64, 32)
+    got_k, got_v = oracle.dequantize_kv(kc, Ck, vc, Cv, lam)
+    assert np.max(np.abs(got_k - k)) < 1e-12 * np.abs(k).max()
+    assert np.array_equal(got_v, v)
+
+
+def test_inverse_key_transform_round_trip():
+    rng = np.random.default_rng(44)
+    k = rng.standard_normal((40, 2, 128))
+    k[:, :, 7] *= 20.0                                    # an outlier channel
+    lam = oracle.smoothing_lambda(k)
+    back = oracle.inverse_transform_keys(oracle.transform_keys(k, lam), lam)
+    assert np.max(np.abs(back - k)) < 1e-12 * np.abs(k).max()
+
+
+def test_attention_over_dequantized_cache_equals_decode_attention():
+    """Dense attention of the raw query over (K^, V^) gives the quantized
+    attention over the codes: q K^T = q~ VQ^-1(K~_q)^T (score rewriting)."""
+    rng = np.random.default_rng(45)
+    N, Hq, Hkv, D = 31, 6, 2, 128
+    Ck, Cv = rng.standard_normal((64, 4)), rng.standard_normal((32, 2))
+    kc = rng.integers(0, 64, (N, Hkv, D // 4)).astype(np.int32)
+    vc = rng.integers(0, 32, (N, Hkv, D // 2)).astype(np.int32)
+    lam = rng.uniform(0.3, 4.0, (Hkv, D))
+    q = rng.standard_normal((Hq, D))
+    k, v = oracle.dequantize_kv(kc, Ck, vc, Cv, lam)
+    out_fp = oracle.attention_fp(q, k, v)
+    out_q = oracle.decode_attention(q, lam, kc, Ck, vc, Cv)
+    assert np.max(np.abs(out_fp - out_q)) < 1e-12
+
+
 def test_attention_single_token_returns_decoded_value():
     rng = np.random.default_rng(19)
     D = 128
