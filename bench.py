@@ -298,6 +298,79 @@ def fp16_comparison(torch, w, dev, steps, l2):
             "padded_tokens_per_sequence": N}
 
 
+def unfused_comparison(torch, vq, w, layout, pools, lam_d, ck_d, cv_d, q_d, num_pages, lens,
+                       steps, dev):
+    """Context, not the product path: the unfused pipeline VecInfer compares its
+    fused kernel against (实验结果, 图5).  Every step dequantises the whole cache
+    of every sequence to dense fp16 K^, V^ with vq_dequantize_kv (sequences
+    padded to the longest, padding rows zero), then runs PyTorch's
+    scaled_dot_product_attention (a library kernel, GQA) over them.  Timed like
+    the step: a CUDA graph of `steps` launches over the rotating pool copies."""
+    import torch.nn.functional as F
+    B, Hq, Hkv, D = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+    N = int(lens.max()) + 1
+    dense_bytes = 2 * B * N * Hkv * D * 2
+    if dense_bytes > 24e9:
+        return {"skipped": "dense fp16 K/V would not fit the memory budget"}
+    slots = np.full((B, N), -1, np.int64)
+    for b, n in enumerate(lens):
+        slots[b, :int(n) + 1] = W.slot_mapping(w, b, 0, int(n) + 1)
+    slots_d = torch.from_numpy(slots.reshape(-1)).to(dev)
+    k_hat = torch.empty((B * N, Hkv, D), dtype=torch.float16, device=dev)
+    v_hat = torch.empty_like(k_hat)
+    k4 = k_hat.view(B, N, Hkv, D).transpose(1, 2)
+    v4 = v_hat.view(B, N, Hkv, D).transpose(1, 2)
+    q4 = q_d.view(B, Hq, 1, D)
+    copies = len(pools)
+
+    def dequant(i):
+        kp, vp = pools[i % copies]
+        vq.vq_dequantize_kv(layout, B * N, slots_d.data_ptr(), lam_d.data_ptr(), ck_d.data_ptr(),
+                            cv_d.data_ptr(), kp.data_ptr(), vp.data_ptr(), num_pages,
+                            k_hat.data_ptr(), v_hat.data_ptr(), None,
+                            torch.cuda.current_stream().cuda_stream)
+
+    def one(i):
+        dequant(i)
+        return F.scaled_dot_product_attention(q4, k4, v4, enable_gqa=True)
+
+    def timed(fn):
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(gr, stream=s):
+                for i in range(steps):
+                    fn(i)
+        torch.cuda.current_stream().wait_stream(s)
+        gr.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        gr.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    ms = timed(one)
+    dq_ms = timed(dequant)
+    code_bytes = B * N * Hkv * (layout_row_bytes(w, "k") + layout_row_bytes(w, "v"))
+    del k_hat, v_hat, k4, v4
+    torch.cuda.empty_cache()
+    return {"pipeline": "vq_dequantize_kv, then torch scaled_dot_product_attention (fp16, enable_gqa)",
+            "us_per_step": ms * 1e3, "dequantize_us": dq_ms * 1e3,
+            "dequantize_gbs": (code_bytes + dense_bytes) / (dq_ms / 1e3) / 1e9,
+            "dense_bytes_per_step": dense_bytes, "padded_tokens_per_sequence": N}
+
+
+def layout_row_bytes(w, which):
+    d, b = (w.k_sub, w.k_bits) if which == "k" else (w.v_sub, w.v_bits)
+    return (-(-(w.head_dim // d) * b // 8) + 3) // 4 * 4
+
+
 def encode_report(w, tokens, ms, sms, clocks):
     """Prefill encode throughput and its roofline.  The encode is bound by the FP32
     pipe: a nearest-centroid scan spends d fused multiply-adds per centroid and
@@ -578,7 +651,7 @@ def main():
                "h2d_bytes_per_step": q_p.numel() * 2 + k_p.numel() * 2 + v_p.numel() * 2,
                "d2h_bytes_per_step": out_p.numel() * 2, "ms_per_step": e_ms}
 
-    comparison = None
+    comparison = unfused = None
     if world == 1 and not args.no_fp16_compare:
         try:
             comparison = fp16_comparison(torch, w, dev, min(K, 200), l2)
@@ -587,6 +660,14 @@ def main():
                 comparison["attention_speedup_vs_fp16"] = comparison["us_per_step"] / (1e3 * split_launch_ms)
         except Exception as exc:  # context only: never fail the bench line on it
             comparison = {"skipped": f"{type(exc).__name__}: {exc}"[:200]}
+        try:
+            unfused = unfused_comparison(torch, vq, w, layout, pools, lam_d, ck_d, cv_d, q_d,
+                                         num_pages, lens, min(K, 200), dev)
+            if "us_per_step" in unfused:
+                unfused["step_speedup_vs_unfused"] = unfused["us_per_step"] / (1e3 * ms_per_step)
+                unfused["dequantize_hbm_frac"] = unfused["dequantize_gbs"] / hbm_peak
+        except Exception as exc:
+            unfused = {"skipped": f"{type(exc).__name__}: {exc}"[:200]}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -614,6 +695,7 @@ def main():
                              "combine": 1e3 * float(np.mean(comb_ms)), "step": 1e3 * ms_per_step},
             "prefill_encode": encode_report(w, prefill_tokens, enc_ms, sms, clocks),
             "fp16_comparison": comparison,
+            "unfused_comparison": unfused,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * K, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -33,7 +33,8 @@ VQ_DEV_OK, VQ_DEV_BAD_PAGE, VQ_DEV_BAD_SLOT, VQ_DEV_TIMEOUT, VQ_DEV_BAD_CONFIG =
 # every symbol include/vqattn.h declares
 EXPORTED = ("vq_code_row_bytes", "vq_check_layout", "vq_encode_kv", "vq_decode_workspace_bytes",
             "vq_default_num_splits", "vq_decode_attention", "vq_decode_partial",
-            "vq_decode_combine", "vq_decode_step", "vq_decode_attention_static", "vq_static_scratch_bytes", "vq_last_error",
+            "vq_decode_combine", "vq_decode_step", "vq_dequantize_kv",
+            "vq_decode_attention_static", "vq_static_scratch_bytes", "vq_last_error",
             "vq_version")
 
 
@@ -75,6 +76,7 @@ def lib() -> ctypes.CDLL:
             "vq_code_row_bytes": (SZ, [I32, I32, I32]),
             "vq_check_layout": (I32, [LP, I32]),
             "vq_encode_kv": (I32, [LP, I32, P, P, P, P, P, P, P, P, I64, P, P]),
+            "vq_dequantize_kv": (I32, [LP, I32, P, P, P, P, P, P, I64, P, P, P, P]),
             "vq_decode_workspace_bytes": (SZ, [LP, I32, I32, I32, I32]),
             "vq_default_num_splits": (I32, [LP, I32, I32, I32]),
             "vq_decode_attention": (I32, [LP, I32, P, P, P, P, P, P, I64, P, I32, P, I32,
@@ -123,6 +125,14 @@ def vq_encode_kv(layout, num_tokens, k, v, slot_mapping, lambda_, codebook_k, co
                               _ptr(slot_mapping), _ptr(lambda_), _ptr(codebook_k),
                               _ptr(codebook_v), _ptr(k_pool), _ptr(v_pool), num_pages,
                               _ptr(status), _ptr(stream)))
+
+
+def vq_dequantize_kv(layout, num_tokens, slot_mapping, lambda_, codebook_k, codebook_v, k_pool,
+                     v_pool, num_pages, k_out, v_out, status=None, stream=None) -> None:
+    _check(lib().vq_dequantize_kv(ctypes.byref(layout), num_tokens, _ptr(slot_mapping),
+                                  _ptr(lambda_), _ptr(codebook_k), _ptr(codebook_v), _ptr(k_pool),
+                                  _ptr(v_pool), num_pages, _ptr(k_out), _ptr(v_out), _ptr(status),
+                                  _ptr(stream)))
 
 
 def vq_decode_workspace_bytes(layout, batch, max_seq_len, num_splits=0, num_sms=0) -> int:
@@ -274,6 +284,35 @@ def encode_kv(layout: vq_layout, k, v, slot_mapping, lambda_, codebook_k, codebo
                  _dev_ptr(v_pool, torch.uint8, "v_pool") if v is not None else None,
                  (k_pool if k is not None else v_pool).shape[0],
                  _dev_ptr(status, torch.int32, "status", (1,)), _stream(stream))
+
+
+def dequantize_kv(layout: vq_layout, slot_mapping, lambda_, codebook_k, codebook_v, k_pool,
+                  v_pool, keys: bool = True, values: bool = True, k_out=None, v_out=None,
+                  status=None, stream=None):
+    """(K^, V^) fp16 [T][Hkv][D] read back from the pools at slot_mapping (int64 [T]);
+    keys in the original space.  A half not asked for is returned as None."""
+    torch = _torch()
+    T = slot_mapping.shape[0]
+    D, H = layout.head_dim, layout.num_kv_heads
+    dev = slot_mapping.device
+    if keys and k_out is None:
+        k_out = torch.empty((T, H, D), dtype=torch.float16, device=dev)
+    if values and v_out is None:
+        v_out = torch.empty((T, H, D), dtype=torch.float16, device=dev)
+    k_out, v_out = (k_out if keys else None), (v_out if values else None)
+    vq_dequantize_kv(layout, T, _dev_ptr(slot_mapping, torch.int64, "slot_mapping", (T,)),
+                     _dev_ptr(lambda_, torch.float32, "lambda", (H, D)) if keys else None,
+                     _dev_ptr(codebook_k, torch.float16, "codebook_k",
+                              (1 << layout.k_bits, layout.k_sub)) if keys else None,
+                     _dev_ptr(codebook_v, torch.float16, "codebook_v",
+                              (1 << layout.v_bits, layout.v_sub)) if values else None,
+                     _dev_ptr(k_pool, torch.uint8, "k_pool") if keys else None,
+                     _dev_ptr(v_pool, torch.uint8, "v_pool") if values else None,
+                     (k_pool if keys else v_pool).shape[0],
+                     _dev_ptr(k_out, torch.float16, "k_out", (T, H, D)) if keys else None,
+                     _dev_ptr(v_out, torch.float16, "v_out", (T, H, D)) if values else None,
+                     _dev_ptr(status, torch.int32, "status", (1,)), _stream(stream))
+    return k_out, v_out
 
 
 def decode_attention(layout: vq_layout, q, lambda_, codebook_k, codebook_v, k_pool, v_pool,

@@ -211,6 +211,56 @@ vq_status vq_encode_kv(const vq_layout* layout, int32_t num_tokens, const void* 
                             "vq_encode_kv launch");
 }
 
+vq_status vq_dequantize_kv(const vq_layout* layout, int32_t num_tokens,
+                           const int64_t* slot_mapping, const float* lambda,
+                           const void* codebook_k, const void* codebook_v, const void* k_pool,
+                           const void* v_pool, int64_t num_pages, void* k_out, void* v_out,
+                           int32_t* status, void* stream) {
+  vq_status st = check_layout_impl(layout, 0);
+  if (st != VQ_OK) return st;
+  const vq_layout& L = *layout;
+  if (num_tokens < 0) return fail(VQ_ERR_INVALID_ARG, "num_tokens %d < 0", num_tokens);
+  if (num_tokens == 0) return VQ_OK;  // empty tensors may come with NULL pointers
+  if (!k_out && !v_out) return fail(VQ_ERR_INVALID_ARG, "k_out and v_out are both NULL");
+  if (!slot_mapping) return fail(VQ_ERR_INVALID_ARG, "slot_mapping is NULL");
+  if (num_pages < 1) return fail(VQ_ERR_INVALID_ARG, "num_pages %lld < 1", (long long)num_pages);
+  if (k_out && (!lambda || !codebook_k || !k_pool))
+    return fail(VQ_ERR_INVALID_ARG, "k_out given but lambda, codebook_k or k_pool is NULL");
+  if (v_out && (!codebook_v || !v_pool))
+    return fail(VQ_ERR_INVALID_ARG, "v_out given but codebook_v or v_pool is NULL");
+  const void* ptrs[] = {k_out, v_out, lambda, codebook_k, codebook_v, k_pool, v_pool, slot_mapping};
+  for (const void* ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return fail(VQ_ERR_INVALID_ARG, "device buffer %p is not 16-byte aligned", ptr);
+
+  vqk::DequantParams p{};
+  p.k_pool = static_cast<const uint8_t*>(k_pool);
+  p.v_pool = static_cast<const uint8_t*>(v_pool);
+  p.cb_k = codebook_k;
+  p.cb_v = codebook_v;
+  p.out_k = k_out;
+  p.out_v = v_out;
+  p.k_sub = L.k_sub;
+  p.k_bits = L.k_bits;
+  p.k_row = static_cast<int>(vq_code_row_bytes(L.head_dim, L.k_sub, L.k_bits));
+  p.v_sub = L.v_sub;
+  p.v_bits = L.v_bits;
+  p.v_row = static_cast<int>(vq_code_row_bytes(L.head_dim, L.v_sub, L.v_bits));
+  p.lambda = lambda;
+  p.slots = slot_mapping;
+  p.status = status;
+  p.num_slots = static_cast<long long>(num_pages) * L.page_size;
+  p.num_tokens = num_tokens;
+  p.hkv = L.num_kv_heads;
+  p.page_size = L.page_size;
+  p.which_base = k_out ? 0 : 1;
+  p.which_last = v_out ? 1 : 0;
+  const int per_cta = vqk::dequant_tokens_per_cta();
+  const int grid_x = (num_tokens + per_cta - 1) / per_cta;
+  cudaError_t e = vqk::launch_dequant(p, grid_x, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "vq_dequantize_kv launch");
+  return VQ_OK;
+}
+
 int32_t vq_default_num_splits(const vq_layout* layout, int32_t batch, int32_t max_seq_len,
                               int32_t num_sms) {
   if (!layout || batch < 0 || max_seq_len < 0 || layout->num_kv_heads < 1) return 0;

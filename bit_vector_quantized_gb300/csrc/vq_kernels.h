@@ -57,6 +57,22 @@ struct DecodeParams {
   float qscale;               // softmax scale * log2(e) / sqrt(128)
 };
 
+struct DequantParams {
+  const uint8_t* k_pool;      // code pools [num_pages][Hkv][P][row bytes]
+  const uint8_t* v_pool;
+  const void* cb_k;           // fp16 [2^bits][sub]
+  const void* cb_v;
+  void* out_k;                // fp16 [T][Hkv][128]
+  void* out_v;
+  int k_sub, k_bits, k_row, v_sub, v_bits, v_row;
+  const float* lambda;        // fp32 [Hkv][128]
+  const int64_t* slots;       // [T]
+  int32_t* status;
+  long long num_slots;        // num_pages * P
+  int num_tokens, hkv, page_size;
+  int which_base, which_last;  // tensors produced: keys (0) and / or values (1)
+};
+
 struct CombineParams {
   const float* ws_o;
   const float2* ws_ml;
@@ -134,5 +150,7 @@ size_t encode_smem_bytes(int sub, int bits);
 cudaError_t launch_decode(const DecodeParams& p, int k_sub, int k_bits, int v_sub, int v_bits,
                           int grid, size_t smem, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+cudaError_t launch_dequant(const DequantParams& p, int grid_x, cudaStream_t stream);
+int dequant_tokens_per_cta();
 
 }  // namespace vqk

@@ -139,6 +139,35 @@ vq_status vq_encode_kv(const vq_layout* layout, int32_t num_tokens,
                        int32_t* status, void* stream);
 
 /*
+ * Dequantise cached tokens back to fp16 keys and values in their original
+ * spaces: the inverse of vq_encode_kv up to the quantisation error (VecInfer,
+ * section 方法细节: a vector is read back as the concatenation of the
+ * centroids its codes name, "注意力机制中的向量量化KV缓存"; keys were coded as
+ * K~ = K diag(lambda)^-1 H_D, "Hadamard引理与注意力分数重写", and H_D is
+ * symmetric and orthonormal).  This is the first half of an unfused pipeline
+ * (dequantise, then dense attention), the baseline the VecInfer page compares
+ * its fused kernel against (实验结果, 图5).
+ *   For each token t and KV head h, with slot = slot_mapping[t]:
+ *     k_out[t][h] = VQ^-1(K code row) H_D diag(lambda[h])  (fp32, rounded to fp16)
+ *     v_out[t][h] = VQ^-1(V code row)                       (exact fp16 centroids)
+ *   k_out, v_out  fp16 [num_tokens][Hkv][D], written in full.  Either may be
+ *                 NULL (that half is not produced), not both.
+ *   slot_mapping  int64 [num_tokens].  A negative slot gives zero rows; a slot
+ *                 >= num_pages * P gives zero rows and reports VQ_DEV_BAD_SLOT.
+ *   lambda        fp32 [Hkv][D]; required when k_out is non-NULL.
+ *   codebooks, pools, num_pages, status: as in vq_encode_kv (the pools are
+ *                 only read).
+ * Supports every format vq_encode_kv supports.  Launched without programmatic
+ * overlap: it starts after the previous work on `stream` has completed.
+ * num_tokens == 0 is a no-op returning VQ_OK.
+ */
+vq_status vq_dequantize_kv(const vq_layout* layout, int32_t num_tokens,
+                           const int64_t* slot_mapping, const float* lambda,
+                           const void* codebook_k, const void* codebook_v, const void* k_pool,
+                           const void* v_pool, int64_t num_pages, void* k_out, void* v_out,
+                           int32_t* status, void* stream);
+
+/*
  * Workspace bytes vq_decode_attention needs for `batch` sequences split
  * `num_splits` ways (num_splits <= 0: the value vq_default_num_splits picks).
  * Pure host arithmetic.  Returns 0 for invalid arguments.
