@@ -1,5 +1,5 @@
 // vq_decode.cu -- split-K fused decode attention over vector-quantized KV codes
-// (sm_103a), and the split-combine kernel.
+// (sm_103a).  The split partials are merged by vq_combine.cu.
 //
 // What is computed (VecInfer, section 方法细节 "注意力机制中的向量量化KV缓存"):
 //   q~ = q diag(lambda) H_D,  s = q~ VQ^-1(K~_q, C_k)^T * scale,
@@ -64,11 +64,6 @@ __device__ __forceinline__ uint2 tab64(uint32_t off) {
 }
 __device__ __forceinline__ uint32_t tab32(uint32_t off) {
   return *reinterpret_cast<const uint32_t*>(g_smem + off);
-}
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
 }
 // Table offset of the 8-bit code in byte i of w: byte 1 of the result is the
 // code (the 256-byte row), byte 0 the lane's byte inside the row (lw < 256).
@@ -833,48 +828,6 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   __syncthreads();  // matches the producers' final barrier
 }
 
-// Merge of the split partials: o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
-// Each thread (one output element) loads all of its (m, l) pairs and partial
-// outputs of a chunk of up to 32 splits before using any (one round trip to
-// L2, bypassing L1: the partials were written by the previous kernel), then
-// merges them; chunks after the first rescale the running sums.  With at most
-// kC splits the sums are formed in split order from the global maximum.
-template <int kC>
-__global__ void __launch_bounds__(kHeadDim) vq_combine_kernel(const CombineParams p) {
-  const int row = blockIdx.x, d = threadIdx.x;
-  pdl_trigger();
-  pdl_wait();
-  const float2* ml = p.ws_ml + static_cast<long long>(row) * p.splits;
-  const float* o = p.ws_o + static_cast<long long>(row) * p.splits * kHeadDim + d;
-  float M = -INFINITY, acc = 0.f, l = 0.f;
-  for (int s0 = 0; s0 < p.splits; s0 += kC) {
-    float2 v[kC];
-    float ov[kC];
-#pragma unroll
-    for (int i = 0; i < kC; ++i) {
-      const int sp = s0 + i;
-      v[i] = sp < p.splits ? __ldcg(ml + sp) : make_float2(-INFINITY, 0.f);
-      ov[i] = sp < p.splits ? __ldcg(o + static_cast<long long>(sp) * kHeadDim) : 0.f;
-    }
-    float Mc = M;
-#pragma unroll
-    for (int i = 0; i < kC; ++i) Mc = fmaxf(Mc, v[i].x);
-    if (Mc == -INFINITY) continue;
-    const float a = fast_exp2(M - Mc);  // 0 while nothing is accumulated yet
-    acc *= a;
-    l *= a;
-#pragma unroll
-    for (int i = 0; i < kC; ++i) {
-      const float f = fast_exp2(v[i].x - Mc);
-      acc = fmaf(f, ov[i], acc);
-      l = fmaf(f, v[i].y, l);
-    }
-    M = Mc;
-  }
-  const float res = l > 0.f ? acc / l : 0.f;
-  static_cast<__half*>(p.out)[static_cast<long long>(row) * kHeadDim + d] = __float2half_rn(res);
-}
-
 template <typename K>
 cudaError_t configure(K kern, size_t smem) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -926,15 +879,6 @@ cudaError_t launch_decode(const DecodeParams& p, int k_sub, int k_bits, int v_su
   VQ_CASE(4, 8, 2, 8)
 #undef VQ_CASE
   return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
-  if (p.rows == 0) return cudaSuccess;
-  // chunk of splits loaded at once: the smallest of 4, 8, 16, 32 that holds them all
-  auto kern = p.splits <= 4 ? vq_combine_kernel<4> : p.splits <= 8 ? vq_combine_kernel<8>
-            : p.splits <= 16 ? vq_combine_kernel<16> : vq_combine_kernel<32>;
-  cudaError_t e = launch_pdl(kern, dim3(p.rows), dim3(kHeadDim), 0, stream, p);
-  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace vqk

@@ -157,6 +157,13 @@ __device__ __forceinline__ void split_half2(float x0, float x1, uint32_t& hi, ui
 // 128-vector spread over a warp: lane l holds elements 4l .. 4l+3.  Butterflies
 // (a, b) -> (a + b, a - b) at strides 1 and 2 in registers, 4 .. 64 across
 // lanes.  Multiply by 1/sqrt(128) for the orthonormal H_128.
+// 2^x with the hardware approximation (ex2.approx.ftz); 2^-inf = 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void fwht128_warp(float (&x)[4], int lane) {
   {
     const float a0 = x[0] + x[1], a1 = x[0] - x[1];
