@@ -69,6 +69,27 @@ __device__ __forceinline__ void centroids(const __half* cb, int d, const uint32_
   }
 }
 
+// Unnormalised Walsh-Hadamard butterflies of one 128-vector held 4 per lane
+// (element 4l + e in x[e] of lane l): 2 stages in registers, 5 by shuffle.
+// Each shuffle stage is one FMA per element: the lower partner keeps x + y,
+// the upper one y - x = fma(-1, x, y), both exact up to the one rounding.
+__device__ __forceinline__ void butterflies(float (&x)[4], int lane) {
+  const float a0 = x[0] + x[1], a1 = x[0] - x[1];
+  const float a2 = x[2] + x[3], a3 = x[2] - x[3];
+  x[0] = a0 + a2;
+  x[2] = a0 - a2;
+  x[1] = a1 + a3;
+  x[3] = a1 - a3;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const float sg = (lane & m) ? -1.f : 1.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[e] = fmaf(sg, x[e], __shfl_xor_sync(0xffffffffu, x[e], m));
+  }
+}
+
+// DK, BK, DV, BV: the formats at compile time (0: read them from the params).
+template <int DK, int BK, int DV, int BV>
 __global__ void __launch_bounds__(kDqWarps * 32, 4) vq_dequant_kernel(const DequantParams p) {
   const int lane = threadIdx.x & 31;
   const int t = static_cast<int>(blockIdx.x) * kDqWarps + (threadIdx.x >> 5);
@@ -86,9 +107,10 @@ __global__ void __launch_bounds__(kDqWarps * 32, 4) vq_dequant_kernel(const Dequ
   int d[2], b[2], rb[2], c0[2], nc[2], wi[2], nw[2];
 #pragma unroll
   for (int w = 0; w < 2; ++w) {
-    d[w] = w ? p.v_sub : p.k_sub;
-    b[w] = w ? p.v_bits : p.k_bits;
-    rb[w] = w ? p.v_row : p.k_row;
+    d[w] = w ? (DV ? DV : p.v_sub) : (DK ? DK : p.k_sub);
+    b[w] = w ? (BV ? BV : p.v_bits) : (BK ? BK : p.k_bits);
+    rb[w] = w ? (DV ? ((kHeadDim / DV) * BV + 31) / 32 * 4 : p.v_row)
+              : (DK ? ((kHeadDim / DK) * BK + 31) / 32 * 4 : p.k_row);
     nc[w] = d[w] >= 4 ? 1 : 4 / d[w];
     c0[w] = d[w] == 8 ? lane >> 1 : lane * nc[w];
     wi[w] = (c0[w] * b[w]) >> 5;
@@ -132,7 +154,7 @@ __global__ void __launch_bounds__(kDqWarps * 32, 4) vq_dequant_kernel(const Dequ
         const int h = h0 + j;
         if (h >= p.hkv) break;  // uniform over the warp
         if (w == 0) {  // K^ = K~ H_D diag(lambda)
-          fwht128_warp(x[j], lane);
+          butterflies(x[j], lane);
           const float4 lam = __ldg(reinterpret_cast<const float4*>(p.lambda + h * kHeadDim) + lane);
           constexpr float kInvSqrtD = 0.08838834764831845f;  // 1 / sqrt(128)
           x[j][0] *= kInvSqrtD * lam.x;
@@ -154,7 +176,16 @@ __global__ void __launch_bounds__(kDqWarps * 32, 4) vq_dequant_kernel(const Dequ
 }  // namespace
 
 cudaError_t launch_dequant(const DequantParams& p, int grid_x, cudaStream_t stream) {
-  vq_dequant_kernel<<<grid_x, kDqWarps * 32, 0, stream>>>(p);
+  // the decode formats at compile time; any other format reads them at run time
+  auto kern = vq_dequant_kernel<0, 0, 0, 0>;
+  const bool k8 = p.k_bits == 8 && (p.k_sub == 2 || p.k_sub == 4);
+  if (k8 && p.v_sub == 4 && p.v_bits == 8)
+    kern = p.k_sub == 4 ? vq_dequant_kernel<4, 8, 4, 8> : vq_dequant_kernel<2, 8, 4, 8>;
+  else if (k8 && p.v_sub == 4 && p.v_bits == 9)
+    kern = p.k_sub == 4 ? vq_dequant_kernel<4, 8, 4, 9> : vq_dequant_kernel<2, 8, 4, 9>;
+  else if (k8 && p.v_sub == 2 && p.v_bits == 8)
+    kern = p.k_sub == 4 ? vq_dequant_kernel<4, 8, 2, 8> : vq_dequant_kernel<2, 8, 2, 8>;
+  kern<<<grid_x, kDqWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
