@@ -52,6 +52,8 @@ def lib():
             "vqo_inverse_transform_keys": (None, [L, I, I, P, P, P, P]),
             "vqo_decode_attention": (None, [L, I, I, I, P, P, P, I, P, P, I, P, P, D, P]),
             "vqo_attention_fp": (None, [L, I, I, I, P, P, P, D, P]),
+            "vqo_decode_attention_residual": (None, [L, L, I, I, I, P, P, P, I, P, P, I, P, P,
+                                                      P, P, D, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(_lib, name)
@@ -233,6 +235,29 @@ def decode_attention(q: np.ndarray, lam: np.ndarray, k_codes: np.ndarray, Ck: np
     scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
     lib().vqo_decode_attention(N, Hq, Hkv, D, _p(q), _p(lam), _p(H), dk, _p(kc), _p(Ck),
                                dv, _p(vc), _p(Cv), scale, _p(out))
+    return out
+
+
+def decode_attention_residual(q: np.ndarray, lam: np.ndarray, k_codes: np.ndarray,
+                              Ck: np.ndarray, v_codes: np.ndarray, Cv: np.ndarray,
+                              k_res: np.ndarray, v_res: np.ndarray,
+                              scale: Optional[float] = None) -> np.ndarray:
+    """fp64 [Hq][D]: one sequence's attention over its codes [N][Hkv][S] and its
+    full-precision residual tokens k_res, v_res [R][Hkv][D], one softmax."""
+    q, lam, Ck, Cv = _f64(q), _f64(lam), _f64(Ck), _f64(Cv)
+    kr, vr = _f64(k_res), _f64(v_res)
+    Hq, D = q.shape
+    kc = np.ascontiguousarray(k_codes, dtype=np.int32)
+    vc = np.ascontiguousarray(v_codes, dtype=np.int32)
+    N, Hkv, _ = kc.shape
+    R = kr.shape[0]
+    dk, dv = Ck.shape[1], Cv.shape[1]
+    H = hadamard(D)
+    out = np.zeros((Hq, D))
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    lib().vqo_decode_attention_residual(N, R, Hq, Hkv, D, _p(q), _p(lam), _p(H), dk, _p(kc),
+                                        _p(Ck), dv, _p(vc), _p(Cv), _p(kr), _p(vr), scale,
+                                        _p(out))
     return out
 
 

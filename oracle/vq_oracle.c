@@ -334,6 +334,69 @@ void vqo_decode_attention(long N, int Hq, int Hkv, int D, const double *q, const
 }
 
 /*
+ * Decode attention over a quantized cache plus a full-precision residual
+ * (VecInfer, 实验结果 / 实验设置: every method keeps a residual of the most
+ * recent tokens, 128, unquantized).  One softmax runs over the N quantized
+ * tokens and the R residual tokens together:
+ *   quantized token t:  s_t = q~ VQ^-1(K~_q)_t^T * scale, value VQ^-1(V_q)_t
+ *                       (q~ = q diag(lambda) H_D, as vqo_decode_attention)
+ *   residual token r:   s_r = q Kr_r^T * scale, value Vr_r (raw fp16 inputs)
+ *   o = sum_t p_t value_t,  p = softmax over all N + R scores.
+ *   kr, vr: [R][Hkv][D]; the other arguments as vqo_decode_attention.
+ * N + R == 0 gives a zero output.
+ */
+void vqo_decode_attention_residual(long N, long R, int Hq, int Hkv, int D, const double *q,
+                                   const double *lam, const double *H, int dk, const int32_t *kc,
+                                   const double *Ck, int dv, const int32_t *vc, const double *Cv,
+                                   const double *kr, const double *vr, double scale, double *out) {
+  const int G = Hq / Hkv, Sk = D / dk, Sv = D / dv;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int h = 0; h < Hq; ++h) {
+    const int kvh = h / G;
+    const double *qh = q + (long)h * D;
+    double *qt = (double *)malloc(sizeof(double) * D);
+    double *kh = (double *)malloc(sizeof(double) * D);
+    double *s = (double *)malloc(sizeof(double) * (N + R > 0 ? N + R : 1));
+    double *o = out + (long)h * D;
+    vqo_transform_query(D, qh, lam + (long)kvh * D, H, qt);
+    for (long t = 0; t < N; ++t) {  /* quantized tokens: transformed query, decoded key */
+      const int32_t *c = kc + (t * Hkv + kvh) * Sk;
+      for (int i = 0; i < Sk; ++i)
+        for (int e = 0; e < dk; ++e) kh[i * dk + e] = Ck[(long)c[i] * dk + e];
+      double acc = 0.0;
+      for (int j = 0; j < D; ++j) acc += qt[j] * kh[j];
+      s[t] = acc * scale;
+    }
+    for (long r = 0; r < R; ++r) {  /* residual tokens: raw query and key */
+      const double *k = kr + (r * Hkv + kvh) * D;
+      double acc = 0.0;
+      for (int j = 0; j < D; ++j) acc += qh[j] * k[j];
+      s[N + r] = acc * scale;
+    }
+    double m = -INFINITY;
+    for (long t = 0; t < N + R; ++t)
+      if (s[t] > m) m = s[t];
+    double l = 0.0;
+    for (int j = 0; j < D; ++j) o[j] = 0.0;
+    for (long t = 0; t < N + R; ++t) {
+      const double p = exp(s[t] - m);
+      l += p;
+      if (t < N) {
+        const int32_t *c = vc + (t * Hkv + kvh) * Sv;
+        for (int i = 0; i < Sv; ++i)
+          for (int e = 0; e < dv; ++e) o[i * dv + e] += p * Cv[(long)c[i] * dv + e];
+      } else {
+        const double *v = vr + ((t - N) * Hkv + kvh) * D;
+        for (int j = 0; j < D; ++j) o[j] += p * v[j];
+      }
+    }
+    if (N + R > 0)
+      for (int j = 0; j < D; ++j) o[j] /= l;
+    free(qt); free(kh); free(s);
+  }
+}
+
+/*
  * Full-precision decode attention (VecInfer, 背景知识 / "KV缓存与注意力机制"):
  * s = q K^T * scale, p = softmax(s), o = p V, on unquantized K and V.
  * K, V: [N][Hkv][D]; q, out: [Hq][D].

@@ -327,6 +327,58 @@ def test_attention_over_dequantized_cache_equals_decode_attention():
     assert np.max(np.abs(out_fp - out_q)) < 1e-12
 
 
+# ---------------------------------------------------- full-precision residual ---
+
+def test_residual_attention_golden_d2():
+    f = _fixture("attention_residual_d2.txt")
+    q = np.array(f["q"][0]).reshape(1, 2)
+    lam = np.array(f["lambda"][0]).reshape(1, 2)
+    Ck = np.array(f["ck"][0]).reshape(2, 2)
+    Cv = np.array(f["cv"][0]).reshape(2, 2)
+    kc = np.array(f["kcode"][0], np.int32).reshape(1, 1, 1)
+    vc = np.array(f["vcode"][0], np.int32).reshape(1, 1, 1)
+    kr = np.array(f["kres"][0]).reshape(1, 1, 2)
+    vr = np.array(f["vres"][0]).reshape(1, 1, 2)
+    out = oracle.decode_attention_residual(q, lam, kc, Ck, vc, Cv, kr, vr)
+    assert np.max(np.abs(out[0] - np.array(f["out"][0]))) < 1e-14
+
+
+def test_residual_attention_reduces_to_its_parts():
+    """No residual: the quantized attention; no codes: textbook attention."""
+    rng = np.random.default_rng(50)
+    N, R, Hq, Hkv, D = 27, 9, 6, 2, 128
+    Ck, Cv = rng.standard_normal((64, 4)), rng.standard_normal((32, 2))
+    kc = rng.integers(0, 64, (N, Hkv, 32)).astype(np.int32)
+    vc = rng.integers(0, 32, (N, Hkv, 64)).astype(np.int32)
+    lam = rng.uniform(0.3, 4.0, (Hkv, D))
+    q = rng.standard_normal((Hq, D))
+    kr, vr = rng.standard_normal((R, Hkv, D)) * 2, rng.standard_normal((R, Hkv, D))
+    none_r = oracle.decode_attention_residual(q, lam, kc, Ck, vc, Cv, kr[:0], vr[:0])
+    assert np.max(np.abs(none_r - oracle.decode_attention(q, lam, kc, Ck, vc, Cv))) < 1e-13
+    none_q = oracle.decode_attention_residual(q, lam, kc[:0], Ck, vc[:0], Cv, kr, vr)
+    for h in range(Hq):
+        kvh = h // (Hq // Hkv)
+        p = scipy.special.softmax(kr[:, kvh] @ q[h] / np.sqrt(D))
+        assert np.max(np.abs(none_q[h] - p @ vr[:, kvh])) < 1e-13
+    empty = oracle.decode_attention_residual(q, lam, kc[:0], Ck, vc[:0], Cv, kr[:0], vr[:0])
+    assert not empty.any()
+
+
+def test_residual_attention_equals_full_attention_over_the_joined_cache():
+    """A cache built from codebook rows, its last R tokens given raw instead of
+    as codes: the same result as full-precision attention over all tokens."""
+    rng = np.random.default_rng(51)
+    N, R, Hq, Hkv, D = 40, 12, 8, 2, 128
+    q, k, v, lam, Ck, Cv, kc, vc = _exact_codebook_case(rng, N, Hq, Hkv, D, 4, 4, 32, 16)
+    out = oracle.decode_attention_residual(q, lam, kc[:N - R], Ck, vc[:N - R], Cv, k[N - R:], v[N - R:])
+    full = np.zeros((Hq, D))
+    for h in range(Hq):
+        kvh = h // (Hq // Hkv)
+        p = scipy.special.softmax(k[:, kvh] @ q[h] / np.sqrt(D))
+        full[h] = p @ v[:, kvh]
+    assert np.max(np.abs(out - full)) < 1e-12
+
+
 def test_attention_single_token_returns_decoded_value():
     rng = np.random.default_rng(19)
     D = 128
