@@ -34,6 +34,7 @@ VQ_DEV_OK, VQ_DEV_BAD_PAGE, VQ_DEV_BAD_SLOT, VQ_DEV_TIMEOUT, VQ_DEV_BAD_CONFIG =
 EXPORTED = ("vq_code_row_bytes", "vq_check_layout", "vq_encode_kv", "vq_decode_workspace_bytes",
             "vq_default_num_splits", "vq_decode_attention", "vq_decode_partial",
             "vq_decode_combine", "vq_decode_step", "vq_dequantize_kv",
+            "vq_decode_residual_workspace_bytes", "vq_decode_attention_residual",
             "vq_decode_attention_static", "vq_static_scratch_bytes", "vq_last_error",
             "vq_version")
 
@@ -77,6 +78,10 @@ def lib() -> ctypes.CDLL:
             "vq_check_layout": (I32, [LP, I32]),
             "vq_encode_kv": (I32, [LP, I32, P, P, P, P, P, P, P, P, I64, P, P]),
             "vq_dequantize_kv": (I32, [LP, I32, P, P, P, P, P, P, I64, P, P, P, P]),
+            "vq_decode_residual_workspace_bytes": (SZ, [LP, I32, I32, I32, I32]),
+            "vq_decode_attention_residual": (I32, [LP, I32, P, P, P, P, P, P, I64, P, I32, P, I32,
+                                                   P, P, P, I32, ctypes.c_float, I32, P, P, SZ,
+                                                   P, P]),
             "vq_decode_workspace_bytes": (SZ, [LP, I32, I32, I32, I32]),
             "vq_default_num_splits": (I32, [LP, I32, I32, I32]),
             "vq_decode_attention": (I32, [LP, I32, P, P, P, P, P, P, I64, P, I32, P, I32,
@@ -133,6 +138,24 @@ def vq_dequantize_kv(layout, num_tokens, slot_mapping, lambda_, codebook_k, code
                                   _ptr(lambda_), _ptr(codebook_k), _ptr(codebook_v), _ptr(k_pool),
                                   _ptr(v_pool), num_pages, _ptr(k_out), _ptr(v_out), _ptr(status),
                                   _ptr(stream)))
+
+
+def vq_decode_residual_workspace_bytes(layout, batch, max_seq_len, num_splits=0, num_sms=0) -> int:
+    return int(lib().vq_decode_residual_workspace_bytes(ctypes.byref(layout), batch, max_seq_len,
+                                                        num_splits, num_sms))
+
+
+def vq_decode_attention_residual(layout, batch, q, lambda_, codebook_k, codebook_v, k_pool,
+                                 v_pool, num_pages, page_table, max_pages_per_seq, seq_lens,
+                                 max_seq_len, k_res, v_res, res_lens, res_capacity, softmax_scale,
+                                 num_splits, out, workspace, workspace_bytes, status=None,
+                                 stream=None) -> None:
+    _check(lib().vq_decode_attention_residual(
+        ctypes.byref(layout), batch, _ptr(q), _ptr(lambda_), _ptr(codebook_k), _ptr(codebook_v),
+        _ptr(k_pool), _ptr(v_pool), num_pages, _ptr(page_table), max_pages_per_seq,
+        _ptr(seq_lens), max_seq_len, _ptr(k_res), _ptr(v_res), _ptr(res_lens), res_capacity,
+        float(softmax_scale), num_splits, _ptr(out), _ptr(workspace), workspace_bytes,
+        _ptr(status), _ptr(stream)))
 
 
 def vq_decode_workspace_bytes(layout, batch, max_seq_len, num_splits=0, num_sms=0) -> int:
@@ -342,6 +365,41 @@ def decode_attention(layout: vq_layout, q, lambda_, codebook_k, codebook_v, k_po
                         _dev_ptr(out, torch.float16, "out", (B, layout.num_q_heads, D)),
                         _dev_ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
                         _dev_ptr(status, torch.int32, "status", (1,)), _stream(stream))
+    return out
+
+
+def decode_attention_residual(layout: vq_layout, q, lambda_, codebook_k, codebook_v, k_pool,
+                              v_pool, page_table, seq_lens, max_seq_len: int, k_res, v_res,
+                              res_lens, out=None, workspace=None, softmax_scale: float = 0.0,
+                              num_splits: int = 0, status=None, stream=None):
+    """fp16 [B][Hq][D] attention of q over the quantized pools (seq_lens tokens)
+    plus the full-precision residual k_res / v_res [B][Hkv][capacity][D]
+    (res_lens tokens), one softmax."""
+    torch = _torch()
+    B = q.shape[0]
+    D, H = layout.head_dim, layout.num_kv_heads
+    cap = k_res.shape[2]
+    if out is None:
+        out = torch.empty((B, layout.num_q_heads, D), dtype=torch.float16, device=q.device)
+    if workspace is None:
+        n = vq_decode_residual_workspace_bytes(layout, B, max_seq_len, num_splits)
+        if n == 0 and B > 0:
+            raise VQError(VQ_ERR_INVALID_ARG, "cannot size the workspace")
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    vq_decode_attention_residual(
+        layout, B, _dev_ptr(q, torch.float16, "q", (B, layout.num_q_heads, D)),
+        _dev_ptr(lambda_, torch.float32, "lambda", (H, D)),
+        _dev_ptr(codebook_k, torch.float16, "codebook_k", (1 << layout.k_bits, layout.k_sub)),
+        _dev_ptr(codebook_v, torch.float16, "codebook_v", (1 << layout.v_bits, layout.v_sub)),
+        _dev_ptr(k_pool, torch.uint8, "k_pool"), _dev_ptr(v_pool, torch.uint8, "v_pool"),
+        k_pool.shape[0], _dev_ptr(page_table, torch.int32, "page_table"), page_table.shape[1],
+        _dev_ptr(seq_lens, torch.int32, "seq_lens", (B,)), max_seq_len,
+        _dev_ptr(k_res, torch.float16, "k_res", (B, H, cap, D)),
+        _dev_ptr(v_res, torch.float16, "v_res", (B, H, cap, D)),
+        _dev_ptr(res_lens, torch.int32, "res_lens", (B,)), cap, softmax_scale, num_splits,
+        _dev_ptr(out, torch.float16, "out", (B, layout.num_q_heads, D)),
+        _dev_ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _dev_ptr(status, torch.int32, "status", (1,)), _stream(stream))
     return out
 
 

@@ -59,6 +59,7 @@ bool decode_formats_supported(const vq_layout& L) {
 }
 
 constexpr int kMaxSplits = 4096;
+constexpr int kMaxResidual = 4096;  // residual window capacity (tokens)
 
 // Split count minimising an estimate of the persistent grid's makespan:
 // waves(units) * (tokens per unit + fixed per-unit cost).
@@ -403,9 +404,23 @@ vq_status launch_partial(const vq_layout& L, const vqk::DecodeParams& p, int gri
   return VQ_OK;
 }
 
+// Residual partials after the split partials of the same workspace.
+struct ResLayout {
+  size_t o_off, ml_off, total;
+};
+
+ResLayout res_layout(const vq_layout& L, int batch, int splits) {
+  ResLayout r;
+  const size_t rows = static_cast<size_t>(batch) * L.num_q_heads;
+  r.o_off = ws_layout(L, batch, splits).total;
+  r.ml_off = r.o_off + ((rows * L.head_dim * sizeof(float) + 255) & ~size_t(255));
+  r.total = r.ml_off + ((rows * 2 * sizeof(float) + 255) & ~size_t(255));
+  return r;
+}
+
 vq_status combine_impl(const vq_layout* layout, int32_t batch, int32_t max_seq_len,
                        int32_t num_splits, const void* workspace, size_t workspace_bytes,
-                       void* out, void* stream) {
+                       void* out, void* stream, bool residual = false) {
   const vq_layout& L = *layout;
   if (!workspace || !out) return fail(VQ_ERR_INVALID_ARG, "workspace or out is NULL");
   if (!aligned16(workspace) || !aligned16(out))
@@ -424,6 +439,13 @@ vq_status combine_impl(const vq_layout* layout, int32_t batch, int32_t max_seq_l
   const uint8_t* wsb = static_cast<const uint8_t*>(workspace);
   cp.ws_o = reinterpret_cast<const float*>(wsb + ws.o_off);
   cp.ws_ml = reinterpret_cast<const float2*>(wsb + ws.ml_off);
+  if (residual) {
+    const ResLayout r = res_layout(L, batch, splits);
+    if (workspace_bytes < r.total)
+      return fail(VQ_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, r.total);
+    cp.res_o = reinterpret_cast<const float*>(wsb + r.o_off);
+    cp.res_ml = reinterpret_cast<const float2*>(wsb + r.ml_off);
+  }
   cp.out = out;
   cp.rows = batch * L.num_q_heads;
   cp.splits = splits;
@@ -632,5 +654,75 @@ size_t vq_static_scratch_bytes(void) { return kStaticScratchBytes; }
 const char* vq_last_error(void) { return g_last_error.c_str(); }
 
 const char* vq_version(void) { return "vqattn 0.1.0 sm_103a"; }
+
+size_t vq_decode_residual_workspace_bytes(const vq_layout* layout, int32_t batch,
+                                          int32_t max_seq_len, int32_t num_splits,
+                                          int32_t num_sms) {
+  if (!layout || batch < 0 || max_seq_len < 0 || layout->num_q_heads < 1) return 0;
+  int splits = num_splits;
+  if (splits <= 0) splits = vq_default_num_splits(layout, batch, max_seq_len, num_sms);
+  if (splits <= 0 || splits > kMaxSplits) return 0;
+  return res_layout(*layout, batch, splits).total;
+}
+
+vq_status vq_decode_attention_residual(const vq_layout* layout, int32_t batch, const void* q,
+                                       const float* lambda, const void* codebook_k,
+                                       const void* codebook_v, const void* k_pool,
+                                       const void* v_pool, int64_t num_pages,
+                                       const int32_t* page_table, int32_t max_pages_per_seq,
+                                       const int32_t* seq_lens, int32_t max_seq_len,
+                                       const void* k_res, const void* v_res,
+                                       const int32_t* res_lens, int32_t res_capacity,
+                                       float softmax_scale, int32_t num_splits, void* out,
+                                       void* workspace, size_t workspace_bytes, int32_t* status,
+                                       void* stream) {
+  vq_status st = check_layout_impl(layout, 1);
+  if (st != VQ_OK) return st;
+  const vq_layout& L = *layout;
+  if (batch < 0) return fail(VQ_ERR_INVALID_ARG, "batch %d < 0", batch);
+  if (batch == 0) return VQ_OK;
+  if (res_capacity < 1 || res_capacity > kMaxResidual)
+    return fail(VQ_ERR_INVALID_ARG, "res_capacity %d not in 1..%d", res_capacity, kMaxResidual);
+  const void* ptrs[] = {out, k_res, v_res, res_lens};
+  const char* names[] = {"out", "k_res", "v_res", "res_lens"};
+  for (int i = 0; i < 4; ++i) {
+    if (!ptrs[i]) return fail(VQ_ERR_INVALID_ARG, "%s is NULL", names[i]);
+    if (!aligned16(ptrs[i])) return fail(VQ_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+  }
+  vqk::DecodeParams p;
+  int grid = 0;
+  size_t smem = 0;
+  st = prepare_decode(layout, batch, q, lambda, codebook_k, codebook_v, k_pool, v_pool, num_pages,
+                      page_table, max_pages_per_seq, seq_lens, max_seq_len, softmax_scale,
+                      num_splits, workspace, workspace_bytes, status, p, grid, smem);
+  if (st != VQ_OK) return st;
+  const ResLayout r = res_layout(L, batch, p.splits);
+  if (workspace_bytes < r.total)
+    return fail(VQ_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, r.total);
+
+  // 1. the residual window's partial, 2. split attention over the codes, 3. merge
+  vqk::ResidualParams rp{};
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  rp.q = q;
+  rp.k_res = k_res;
+  rp.v_res = v_res;
+  rp.res_lens = res_lens;
+  rp.res_o = reinterpret_cast<float*>(wsb + r.o_off);
+  rp.res_ml = reinterpret_cast<float2*>(wsb + r.ml_off);
+  const float scale = softmax_scale == 0.f ? 1.f / std::sqrt(static_cast<float>(L.head_dim)) : softmax_scale;
+  rp.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  rp.hq = L.num_q_heads;
+  rp.hkv = L.num_kv_heads;
+  rp.group = L.num_q_heads / L.num_kv_heads;
+  rp.capacity = res_capacity;
+  const long long rgrid = static_cast<long long>(batch) * L.num_kv_heads;
+  if (rgrid > 0x7fffffffLL) return fail(VQ_ERR_INVALID_ARG, "batch %d too large", batch);
+  cudaError_t e = vqk::launch_residual(rp, static_cast<int>(rgrid), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "residual attention kernel");
+  st = launch_partial(L, p, grid, smem, stream);
+  if (st != VQ_OK) return st;
+  return combine_impl(layout, batch, max_seq_len, p.splits, workspace, workspace_bytes, out, stream,
+                      true);
+}
 
 }  // extern "C"

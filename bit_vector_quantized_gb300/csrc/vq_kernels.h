@@ -76,9 +76,22 @@ struct DequantParams {
 struct CombineParams {
   const float* ws_o;
   const float2* ws_ml;
+  const float* res_o;         // optional residual partials [B * Hq][128] (NULL: none)
+  const float2* res_ml;       // [B * Hq], merged as split number `splits`
   void* out;                  // fp16 [B][Hq][128]
   int rows;                   // B * Hq
   int splits;
+};
+
+struct ResidualParams {
+  const void* q;              // fp16 [B][Hq][128]
+  const void* k_res;          // fp16 [B][Hkv][capacity][128]
+  const void* v_res;
+  const int32_t* res_lens;    // [B], clamped to [0, capacity]
+  float* res_o;               // fp32 [B * Hq][128]
+  float2* res_ml;             // [B * Hq]: (m, l), log2 domain
+  float scale_log2;           // softmax scale * log2(e)
+  int hq, hkv, group, capacity;
 };
 
 constexpr int kProducerWarps = 4;  // TMA-issuing warps (one in four stages each)
@@ -151,6 +164,8 @@ cudaError_t launch_decode(const DecodeParams& p, int k_sub, int k_bits, int v_su
                           int grid, size_t smem, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 cudaError_t launch_dequant(const DequantParams& p, int grid_x, cudaStream_t stream);
+cudaError_t launch_residual(const ResidualParams& p, int grid, cudaStream_t stream);
+size_t residual_smem_bytes(int group, int capacity);
 int dequant_tokens_per_cta();
 
 }  // namespace vqk

@@ -276,6 +276,45 @@ vq_status vq_decode_step(const vq_layout* layout, int32_t batch, const void* q, 
                          int32_t* status, void* stream);
 
 /*
+ * Decode attention over a quantized cache plus a full-precision residual
+ * window of the most recent tokens (VecInfer, section 实验结果 / 实验设置:
+ * every method keeps a residual of 128 unquantized tokens).  The quantized
+ * tokens score as in vq_decode_attention (s = q~ VQ^-1(K~_q)^T * scale); a
+ * residual token scores with the raw query and key, s = q k^T * scale, and
+ * both join one softmax: o = softmax(s) [VQ^-1(V_q); V_res].
+ *   seq_lens      int32 [batch]: quantized tokens of each sequence (as in
+ *                 vq_decode_attention; 0 is allowed).
+ *   k_res, v_res  fp16 [batch][Hkv][res_capacity][D]: the residual tokens of
+ *                 sequence b and KV head h are rows 0 .. res_lens[b] - 1 of
+ *                 [b][h] (their order does not matter).
+ *   res_lens      int32 [batch], clamped to [0, res_capacity].
+ *   res_capacity  1 .. 4096.
+ *   workspace     at least vq_decode_residual_workspace_bytes(layout, batch,
+ *                 max_seq_len, num_splits, 0) bytes, 256-byte aligned.
+ * Three kernels on `stream`: the residual partial (one CTA per sequence and KV
+ * head), the split attention over the codes, and the merge, which takes the
+ * residual partial as one more split.  Moving tokens from the residual into
+ * the cache (vq_encode_kv) is the caller's policy.  Other arguments and errors
+ * as in vq_decode_attention.  A sequence with no token at all gives a zero
+ * row.
+ */
+size_t vq_decode_residual_workspace_bytes(const vq_layout* layout, int32_t batch,
+                                          int32_t max_seq_len, int32_t num_splits,
+                                          int32_t num_sms);
+
+vq_status vq_decode_attention_residual(const vq_layout* layout, int32_t batch, const void* q,
+                                       const float* lambda, const void* codebook_k,
+                                       const void* codebook_v, const void* k_pool,
+                                       const void* v_pool, int64_t num_pages,
+                                       const int32_t* page_table, int32_t max_pages_per_seq,
+                                       const int32_t* seq_lens, int32_t max_seq_len,
+                                       const void* k_res, const void* v_res,
+                                       const int32_t* res_lens, int32_t res_capacity,
+                                       float softmax_scale, int32_t num_splits, void* out,
+                                       void* workspace, size_t workspace_bytes, int32_t* status,
+                                       void* stream);
+
+/*
  * Decode attention for callers that cannot allocate device memory.
  *
  * No counterpart on the VecInfer pages: this is a deployment variant of
