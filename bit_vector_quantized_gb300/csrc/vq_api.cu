@@ -55,7 +55,8 @@ bool decode_formats_supported(const vq_layout& L) {
   const bool k_ok = (L.k_sub == 2 || L.k_sub == 4) && L.k_bits == 8;
   const bool v_ok = (L.v_sub == 4 && (L.v_bits == 8 || L.v_bits == 9)) ||
                     (L.v_sub == 2 && L.v_bits == 8);
-  return k_ok && v_ok;
+  const bool wide = L.k_sub == 8 && L.k_bits == 12 && L.v_sub == 8 && L.v_bits == 12;
+  return (k_ok && v_ok) || wide;
 }
 
 constexpr int kMaxSplits = 4096;
@@ -119,8 +120,8 @@ vq_status check_layout_impl(const vq_layout* L, int for_decode) {
     return fail(VQ_ERR_INVALID_ARG, "page_size %d must be a positive multiple of 16", L->page_size);
   if (for_decode && !decode_formats_supported(*L))
     return fail(VQ_ERR_UNSUPPORTED,
-                "decode attention implements (k_sub,k_bits) in {(2,8),(4,8)} and (v_sub,v_bits) "
-                "in {(2,8),(4,8),(4,9)}; got (%d,%d) and (%d,%d)",
+                "decode attention implements (k_sub,k_bits) in {(2,8),(4,8)} with (v_sub,v_bits) "
+                "in {(2,8),(4,8),(4,9)}, and (8,12) with (8,12); got (%d,%d) and (%d,%d)",
                 L->k_sub, L->k_bits, L->v_sub, L->v_bits);
   return VQ_OK;
 }

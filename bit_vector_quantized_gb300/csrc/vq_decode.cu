@@ -135,6 +135,53 @@ struct VCodes<2, 8> {
   }
 };
 
+// d = 8, 12-bit codes (the pages' 1.5-bit configuration): the table is not
+// replicated (4096 rows of 32 bytes: K centroid j in bytes 0..15, V centroid j
+// in bytes 16..31), so a gather is (code << 5) | half | tensor.  A lane's
+// 8-byte gather is half of one 8-element centroid.
+__device__ __forceinline__ uint32_t row12(uint32_t code, uint32_t lw, int half) {
+  return (code << 5) | lw | (static_cast<uint32_t>(half) << 3);
+}
+template <>
+struct KCodes<8> {
+  uint32_t a, b;  // the lane's 48-bit code group (sub-vectors 4c .. 4c+3), from bit 0
+  __device__ __forceinline__ void load(const uint8_t* row, int c) {
+    // codes 4c .. 4c+3 sit at bits 48c .. 48c+47: words w0, w0+1, shift 0 or 16
+    const uint32_t* rw = reinterpret_cast<const uint32_t*>(row);
+    const int w0 = (48 * c) >> 5;
+    const uint32_t lo = rw[w0], hi = rw[w0 + 1];
+    const uint32_t sh = (48 * c) & 31;
+    a = __funnelshift_r(lo, hi, sh);
+    b = hi >> sh;
+  }
+  // k-step i (0..7) reads half (i & 1) of sub-vector 4c + i / 2
+  __device__ __forceinline__ uint32_t off(int i, uint32_t lw) const {
+    const int j = i >> 1;
+    const uint32_t code = j == 0 ? (a & 0xfffu) : j == 1 ? ((a >> 12) & 0xfffu)
+                        : j == 2 ? (__funnelshift_r(a, b, 24) & 0xfffu) : ((b >> 4) & 0xfffu);
+    return row12(code, lw, i & 1);
+  }
+};
+template <>
+struct VCodes<8, 12> {
+  uint32_t x;  // the lane's 24-bit code pair (sub-vectors 2r, 2r+1), from bit 0
+  __device__ __forceinline__ void load(const uint8_t* row, int r) {
+    // codes 2r, 2r+1 sit at bits 24r .. 24r+23 of the 24-byte row; the next
+    // word is needed only when they cross a word boundary (never for r = 7)
+    const uint32_t* rw = reinterpret_cast<const uint32_t*>(row);
+    const int w0 = (24 * r) >> 5;
+    const uint32_t sh = (24 * r) & 31;
+    const uint32_t lo = rw[w0];
+    const uint32_t hi = sh > 8 ? rw[w0 + 1] : 0u;
+    x = __funnelshift_r(lo, hi, sh);
+  }
+  // output step i (0..3): dims 16r + 4i .. 16r + 4i + 3 = half (i & 1) of sub-vector 2r + i / 2
+  __device__ __forceinline__ uint32_t off(int i, uint32_t lw) const {
+    const uint32_t code = (i >> 1) ? ((x >> 12) & 0xfffu) : (x & 0xfffu);
+    return row12(code, lw, i & 1);
+  }
+};
+
 struct UnitId {
   int b, kvh, s;
 };
@@ -188,7 +235,9 @@ __device__ __forceinline__ UnitStages unit_stages(const DecodeParams& p, int k, 
 
 template <int DK, int BK, int DV, int BV, int NG, int NW, int kNCH>
 __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split_kernel(const DecodeParams p) {
-  static_assert(BK == 8, "K codes are byte-aligned in this build");
+  static_assert(BK == 8 || (DK == 8 && BK == 12 && DV == 8 && BV == 12),
+                "K codes are byte-aligned, or the 1.5-bit format (d = 8, 12-bit codes)");
+  constexpr bool kWide = DK == 8;            // 1.5-bit format: 32-byte table rows, no replicas
   static_assert(NG == 4 || NG == 8, "query heads per pass");
   static_assert(kNCH == 1 || kNCH == 2, "chunks per consumer warp");
   constexpr int NGL = NG == 4 ? 1 : 2;       // heads owned by one lane
@@ -388,13 +437,15 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
 
   // ============================= consumer warps ==============================
   constexpr int kConsumerThreads = NW * 32;
-  constexpr int kNK = ((1 << BK) + kConsumerThreads - 1) / kConsumerThreads;
-  constexpr int kNV = ((1 << BV) + kConsumerThreads - 1) / kConsumerThreads;
+  // replicated tables: each thread's centroids are loaded here, stored after
+  // the query loads have gone out (the wide table is copied in one pass below)
+  constexpr int kNK = kWide ? 1 : ((1 << BK) + kConsumerThreads - 1) / kConsumerThreads;
+  constexpr int kNV = kWide ? 1 : ((1 << BV) + kConsumerThreads - 1) / kConsumerThreads;
   uint2 cbk_r[kNK], cbv_r[kNV];
 #pragma unroll
   for (int i = 0; i < kNK; ++i) {
     const int j = tid + i * kConsumerThreads;
-    if (j < (1 << BK)) {
+    if (!kWide && j < (1 << BK)) {
       if constexpr (DK == 4) cbk_r[i] = __ldg(reinterpret_cast<const uint2*>(p.cb_k) + j);
       else cbk_r[i].x = __ldg(reinterpret_cast<const uint32_t*>(p.cb_k) + j);
     }
@@ -402,7 +453,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
 #pragma unroll
   for (int i = 0; i < kNV; ++i) {
     const int j = tid + i * kConsumerThreads;
-    if (j < (1 << BV)) {
+    if (!kWide && j < (1 << BV)) {
       if constexpr (DV == 4) cbv_r[i] = __ldg(reinterpret_cast<const uint2*>(p.cb_v) + j);
       else cbv_r[i].x = __ldg(reinterpret_cast<const uint32_t*>(p.cb_v) + j);
     }
@@ -421,8 +472,32 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
     }
   };
   load_q(0);
-  {  // codebook table: row j = 16 copies of 8-byte (32 copies of 4-byte) K centroid j,
-     // then the same for V centroid j
+  if constexpr (kWide) {  // table row j = K centroid j (16 bytes), V centroid j (16 bytes)
+    const uint32_t tab = smem_addr(smem + L.tab);
+    constexpr int kBatch = 4;  // loads in flight per thread
+    for (int j0 = tid; j0 < (1 << BK); j0 += kBatch * kConsumerThreads) {
+      uint4 kv[kBatch][2];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int j = j0 + i * kConsumerThreads;
+        if (j < (1 << BK)) {
+          kv[i][0] = __ldg(reinterpret_cast<const uint4*>(p.cb_k) + j);
+          kv[i][1] = __ldg(reinterpret_cast<const uint4*>(p.cb_v) + j);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int j = j0 + i * kConsumerThreads;
+        if (j < (1 << BK)) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(tab + j * kTabRowWide + 16 * t),
+                         "r"(kv[i][t].x), "r"(kv[i][t].y), "r"(kv[i][t].z), "r"(kv[i][t].w));
+        }
+      }
+    }
+  } else {  // codebook table: row j = 16 copies of 8-byte (32 copies of 4-byte) K centroid j,
+            // then the same for V centroid j
     const uint32_t tab = smem_addr(smem + L.tab);
 #pragma unroll
     for (int i = 0; i < kNK; ++i) {
@@ -463,8 +538,8 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   const int r = lane >> 2, c = lane & 3;
   // the lane's byte inside a table row: its replica of the K (bytes 0..127)
   // or V (bytes 128..255) centroid, one bank pair (8-byte) or bank (4-byte) per lane
-  const uint32_t lwk = DK == 4 ? (lane & 15) * 8 : lane * 4;
-  const uint32_t lwv = 128 + (DV == 4 ? (lane & 15) * 8 : lane * 4);
+  const uint32_t lwk = kWide ? 0u : DK == 4 ? (lane & 15) * 8 : lane * 4;
+  const uint32_t lwv = kWide ? 16u : 128 + (DV == 4 ? (lane & 15) * 8 : lane * 4);
   uint32_t qa[8][2];  // score B operands: NG == 4: columns (2g: hi, 2g+1: lo); NG == 8: hi
   uint32_t qb[8][2];  // NG == 8: lo
   float O[8][4];      // output accumulators (NG == 4 uses O[0..3])
@@ -517,7 +592,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {  // tokens 8ks + c and 8ks + c + 4
           uint32_t a0, a1, a2, a3;
-          if constexpr (DV == 4) {
+          if constexpr (DV >= 4) {
             const uint2 w0 = tab64(pvc[n][2 * ks].off(q, lwv));
             const uint2 w1 = tab64(pvc[n][2 * ks + 1].off(q, lwv));
             a0 = w0.x; a1 = w0.y; a2 = w1.x; a3 = w1.y;
@@ -530,7 +605,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
           mma16816(O[q], a0, a1, a2, a3, pb[n][ks][0], pb[n][ks][1]);
         }
       } else {
-        if constexpr (DV == 4) {  // q = output step pair (2q, 2q+1)
+        if constexpr (DV >= 4) {  // q = output step pair (2q, 2q+1)
           uint2 W[4];
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) W[jj] = tab64(pvc[n][jj].off(q, lwv));
@@ -571,7 +646,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
 #pragma unroll
         for (int n = 0; n < kNCH; ++n) {
           uint32_t a0, a1, a2, a3;
-          if constexpr (DK == 4) {
+          if constexpr (DK >= 4) {
             const uint2 g0 = tab64(kc[n][0].off(kk, lwk));
             const uint2 g1 = tab64(kc[n][1].off(kk, lwk));
             a0 = g0.x; a1 = g1.x; a2 = g0.y; a3 = g1.y;
@@ -877,6 +952,7 @@ cudaError_t launch_decode(const DecodeParams& p, int k_sub, int k_bits, int v_su
   VQ_CASE(4, 8, 4, 9)
   VQ_CASE(2, 8, 2, 8)
   VQ_CASE(4, 8, 2, 8)
+  VQ_CASE(8, 12, 8, 12)
 #undef VQ_CASE
   return cudaErrorInvalidValue;
 }

@@ -109,12 +109,14 @@ struct DecodeShape {
 // `warps` is the number of consumer warps.  The codebook table comes first (at
 // offset 0 of the dynamic shared memory): row j is 256 bytes, the replicas of K
 // centroid j in bytes 0..127 and those of V centroid j in bytes 128..255, so a
-// gather address is (code << 8) | lane byte.
+// gather address is (code << 8) | lane byte.  The 1.5-bit format (4096
+// centroids of 8 elements) has 32-byte rows without replicas instead.
 struct DecodeSmem {
   int tab, qt, merge, ml, units, meta, bar, flag, stage, total;
 };
 
-constexpr int kTabRow = 256;  // bytes per codebook table row
+constexpr int kTabRow = 256;      // bytes per codebook table row (replicated centroids)
+constexpr int kTabRowWide = 32;   // 1.5-bit format (12-bit codes): K | V centroid, no replicas
 
 __host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
 
@@ -123,7 +125,7 @@ __host__ __device__ inline DecodeSmem decode_smem(int k_bits, int v_bits, int gr
   DecodeSmem s;
   int o = 0;
   const int rows = 1 << (k_bits > v_bits ? k_bits : v_bits);
-  s.tab = o; o = align128(o + rows * kTabRow);
+  s.tab = o; o = align128(o + rows * (k_bits == 12 ? kTabRowWide : kTabRow));
   s.qt = o; o = align128(o + group * 128 * 4);
   s.merge = o; o = align128(o + warps * group * 128 * 4);
   s.ml = o; o = align128(o + warps * group * 8);

@@ -35,7 +35,10 @@ def _oracle_out(w, cal, refs, q, lens=None):
     return np.stack(outs)
 
 
-DECODE_FORMATS = [(2, 8, 4, 8), (4, 8, 4, 8), (2, 8, 4, 9), (4, 8, 4, 9), (2, 8, 2, 8), (4, 8, 2, 8)]
+# (k_sub, k_bits, v_sub, v_bits): the 2-bit and mixed formats, and the pages'
+# 1.5-bit configuration (4096 centroids of 8 elements, 12-bit codes)
+DECODE_FORMATS = [(2, 8, 4, 8), (4, 8, 4, 8), (2, 8, 4, 9), (4, 8, 4, 9), (2, 8, 2, 8), (4, 8, 2, 8),
+                  (8, 12, 8, 12)]
 
 
 @pytest.mark.parametrize("group", [1, 2, 4, 5, 8])

@@ -19,7 +19,7 @@ def _check_seq(gc, w, cal, b, start, stop, name, log):
 
 FORMATS = [  # (k_sub, k_bits, v_sub, v_bits)
     (2, 8, 4, 8), (4, 8, 4, 8), (2, 8, 4, 9), (4, 8, 2, 8),
-    (1, 4, 8, 10), (8, 12, 1, 3), (4, 9, 2, 1), (2, 6, 4, 5),
+    (1, 4, 8, 10), (8, 12, 1, 3), (4, 9, 2, 1), (2, 6, 4, 5), (8, 12, 8, 12),
 ]
 
 
