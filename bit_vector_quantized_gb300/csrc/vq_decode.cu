@@ -136,11 +136,13 @@ struct VCodes<2, 8> {
 };
 
 // d = 8, 12-bit codes (the pages' 1.5-bit configuration): the table is not
-// replicated (4096 rows of 32 bytes: K centroid j in bytes 0..15, V centroid j
-// in bytes 16..31), so a gather is (code << 5) | half | tensor.  A lane's
-// 8-byte gather is half of one 8-element centroid.
+// replicated.  A lane's 8-byte gather is half of one 8-element centroid, and
+// every lane of one gather reads the same half, so the table is half-major:
+// [tensor][half][code] x 8 bytes (K at 0, V at 64 KiB; half 1 at +32 KiB).
+// Consecutive codes then sit in consecutive bank pairs, and the random codes
+// of a warp spread over all 16 of them.
 __device__ __forceinline__ uint32_t row12(uint32_t code, uint32_t lw, int half) {
-  return (code << 5) | lw | (static_cast<uint32_t>(half) << 3);
+  return (code << 3) | lw | (static_cast<uint32_t>(half) << 15);
 }
 template <>
 struct KCodes<8> {
@@ -472,7 +474,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
     }
   };
   load_q(0);
-  if constexpr (kWide) {  // table row j = K centroid j (16 bytes), V centroid j (16 bytes)
+  if constexpr (kWide) {  // half-major table: [tensor][half][code] x 8 bytes (see row12)
     const uint32_t tab = smem_addr(smem + L.tab);
     constexpr int kBatch = 4;  // loads in flight per thread
     for (int j0 = tid; j0 < (1 << BK); j0 += kBatch * kConsumerThreads) {
@@ -490,9 +492,12 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
         const int j = j0 + i * kConsumerThreads;
         if (j < (1 << BK)) {
 #pragma unroll
-          for (int t = 0; t < 2; ++t)
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(tab + j * kTabRowWide + 16 * t),
-                         "r"(kv[i][t].x), "r"(kv[i][t].y), "r"(kv[i][t].z), "r"(kv[i][t].w));
+          for (int t = 0; t < 2; ++t) {
+            const uint32_t base = tab + t * 65536u + j * 8u;
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(base), "r"(kv[i][t].x), "r"(kv[i][t].y));
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(base + 32768u), "r"(kv[i][t].z),
+                         "r"(kv[i][t].w));
+          }
         }
       }
     }
@@ -539,7 +544,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   // the lane's byte inside a table row: its replica of the K (bytes 0..127)
   // or V (bytes 128..255) centroid, one bank pair (8-byte) or bank (4-byte) per lane
   const uint32_t lwk = kWide ? 0u : DK == 4 ? (lane & 15) * 8 : lane * 4;
-  const uint32_t lwv = kWide ? 16u : 128 + (DV == 4 ? (lane & 15) * 8 : lane * 4);
+  const uint32_t lwv = kWide ? 65536u : 128 + (DV == 4 ? (lane & 15) * 8 : lane * 4);
   uint32_t qa[8][2];  // score B operands: NG == 4: columns (2g: hi, 2g+1: lo); NG == 8: hi
   uint32_t qb[8][2];  // NG == 8: lo
   float O[8][4];      // output accumulators (NG == 4 uses O[0..3])

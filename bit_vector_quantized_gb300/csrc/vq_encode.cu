@@ -43,29 +43,84 @@ __device__ __forceinline__ void scan_centroids(const float (&x)[4], const float*
     best[s] = INFINITY;
     idx[s] = 0x7fffffff;
   }
+  // d = 8 and d = 4: four centroids per iteration, their scores formed
+  // independently (each with the same operations as one at a time), then
+  // compared in index order, so the result is that of the plain loop.
   if constexpr (D == 8) {
-    const int half = (lane & 1) * 4;
-    for (int j = j0; j < j1; ++j) {
-      const float4 c = *reinterpret_cast<const float4*>(cmul + j * 8 + half);
-      float part = x[0] * c.x;
-      part = fmaf(x[1], c.y, part);
-      part = fmaf(x[2], c.z, part);
-      part = fmaf(x[3], c.w, part);
-      const float other = __shfl_xor_sync(0xffffffffu, part, 1);
-      const float s = cnorm[j] + (part + other);
-      if (s < best[0]) {
-        best[0] = s;
+    // Lanes 2i and 2i+1 hold elements 0..3 and 4..7 of sub-vector i.  Each
+    // takes the whole sub-vector (its partner's half by shuffle) and scans
+    // every other centroid, lane 2i the even ones, lane 2i+1 the odd ones; the
+    // score is ||c||^2 + (lo + hi) with lo, hi the dot products of the two
+    // halves, and the pair keeps the lower score (lower index on a tie).
+    const int par = lane & 1;
+    float xa[4], xb[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float o = __shfl_xor_sync(0xffffffffu, x[e], 1);
+      xa[e] = par ? o : x[e];
+      xb[e] = par ? x[e] : o;
+    }
+    auto score = [&](int j) {
+      const float4 c0 = *reinterpret_cast<const float4*>(cmul + j * 8);
+      const float4 c1 = *reinterpret_cast<const float4*>(cmul + j * 8 + 4);
+      float lo = xa[0] * c0.x;
+      lo = fmaf(xa[1], c0.y, lo);
+      lo = fmaf(xa[2], c0.z, lo);
+      lo = fmaf(xa[3], c0.w, lo);
+      float hi = xb[0] * c1.x;
+      hi = fmaf(xb[1], c1.y, hi);
+      hi = fmaf(xb[2], c1.z, hi);
+      hi = fmaf(xb[3], c1.w, hi);
+      return cnorm[j] + (lo + hi);
+    };
+    int j = j0 + ((j0 & 1) != par ? 1 : 0);  // this lane's first centroid of its parity
+    for (; j + 6 < j1; j += 8) {
+      float sc[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) sc[u] = score(j + 2 * u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (sc[u] < best[0]) {
+          best[0] = sc[u];
+          idx[0] = j + 2 * u;
+        }
+    }
+    for (; j < j1; j += 2) {
+      const float sv = score(j);
+      if (sv < best[0]) {
+        best[0] = sv;
         idx[0] = j;
       }
     }
+    const float ob = __shfl_xor_sync(0xffffffffu, best[0], 1);
+    const int oi = __shfl_xor_sync(0xffffffffu, idx[0], 1);
+    if (ob < best[0] || (ob == best[0] && oi < idx[0])) {
+      best[0] = ob;
+      idx[0] = oi;
+    }
   } else if constexpr (D == 4) {
-    for (int j = j0; j < j1; ++j) {
+    auto score = [&](int j) {
       const float4 c = *reinterpret_cast<const float4*>(cmul + j * 4);
       float s = cnorm[j];
       s = fmaf(x[0], c.x, s);
       s = fmaf(x[1], c.y, s);
       s = fmaf(x[2], c.z, s);
-      s = fmaf(x[3], c.w, s);
+      return fmaf(x[3], c.w, s);
+    };
+    int j = j0;
+    for (; j + 4 <= j1; j += 4) {
+      float sc[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) sc[u] = score(j + u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (sc[u] < best[0]) {
+          best[0] = sc[u];
+          idx[0] = j + u;
+        }
+    }
+    for (; j < j1; ++j) {
+      const float s = score(j);
       if (s < best[0]) {
         best[0] = s;
         idx[0] = j;
@@ -362,6 +417,22 @@ __device__ void encode_multi(const EncodeParams& p, int which, const float* cmul
   for (int v = 0; v < NV; ++v) pack_store<D>(p, which, idx[v], act[v], hh[v], slot[v]);
 }
 
+// Centroid j (d fp16 elements, d in {1, 2, 4, 8}) with one load.
+__device__ __forceinline__ void load_centroid(const __half* cb, int j, int d, __half (&c)[8]) {
+  if (d == 8) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(cb) + j);
+    memcpy(c, &u, 16);
+  } else if (d == 4) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(cb) + j);
+    memcpy(c, &u, 8);
+  } else if (d == 2) {
+    const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(cb) + j);
+    memcpy(c, &u, 4);
+  } else {
+    c[0] = __ldg(cb + j);
+  }
+}
+
 __global__ void __launch_bounds__(kEncWarps * 32) vq_encode_kernel(const EncodeParams p) {
   extern __shared__ __align__(16) float enc_smem[];
   const int which = blockIdx.y + p.which_base;
@@ -375,15 +446,31 @@ __global__ void __launch_bounds__(kEncWarps * 32) vq_encode_kernel(const EncodeP
   // the vector's loads go out first, so they overlap the codebook loads below
   VecIn in{};
   if (p.vec_per_warp != kMultiVec) in = load_vector(p, which);
+  // the codebook table: each thread loads four centroids (one vector load
+  // each) before it uses any, so a large codebook costs a few L2 round trips
   const __half* cb = static_cast<const __half*>(p.cb[which]);
-  for (int j = threadIdx.x; j < ncent; j += blockDim.x) {
-    float n = 0.f;
-    for (int e = 0; e < d; ++e) {
-      const float c = __half2float(cb[j * d + e]);
-      cmul[j * d + e] = -2.f * c;
-      n = fmaf(c, c, n);
+  constexpr int kPrepBatch = 4;
+  for (int j0 = threadIdx.x; j0 < ncent; j0 += kPrepBatch * blockDim.x) {
+    __half c[kPrepBatch][8];
+#pragma unroll
+    for (int u = 0; u < kPrepBatch; ++u) {
+      const int j = j0 + u * static_cast<int>(blockDim.x);
+      if (j < ncent) load_centroid(cb, j, d, c[u]);
     }
-    cnorm[j] = n;
+#pragma unroll
+    for (int u = 0; u < kPrepBatch; ++u) {
+      const int j = j0 + u * static_cast<int>(blockDim.x);
+      if (j >= ncent) break;
+      float n = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (e >= d) break;
+        const float v = __half2float(c[u][e]);
+        cmul[j * d + e] = -2.f * v;
+        n = fmaf(v, v, n);
+      }
+      cnorm[j] = n;
+    }
   }
   if (p.vec_per_warp == kMultiVec) {  // prefill: several vectors per warp (sub-vector length 2 or 4)
     if (d == 4) encode_multi<4, kMultiVec>(p, which, cmul, cnorm);

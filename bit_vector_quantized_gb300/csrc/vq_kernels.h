@@ -110,13 +110,14 @@ struct DecodeShape {
 // offset 0 of the dynamic shared memory): row j is 256 bytes, the replicas of K
 // centroid j in bytes 0..127 and those of V centroid j in bytes 128..255, so a
 // gather address is (code << 8) | lane byte.  The 1.5-bit format (4096
-// centroids of 8 elements) has 32-byte rows without replicas instead.
+// centroids of 8 elements) has no replicas: 32 bytes per centroid index, laid
+// out half-major ([tensor][half][code] x 8 bytes).
 struct DecodeSmem {
   int tab, qt, merge, ml, units, meta, bar, flag, stage, total;
 };
 
 constexpr int kTabRow = 256;      // bytes per codebook table row (replicated centroids)
-constexpr int kTabRowWide = 32;   // 1.5-bit format (12-bit codes): K | V centroid, no replicas
+constexpr int kTabRowWide = 32;   // 1.5-bit format (12-bit codes): K and V centroid, no replicas
 
 __host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
 

@@ -107,8 +107,9 @@ size_t vq_code_row_bytes(int32_t head_dim, int32_t sub, int32_t bits);
  * Checks a layout against what this build implements.  VQ_OK, or
  * VQ_ERR_INVALID_ARG / VQ_ERR_UNSUPPORTED with vq_last_error() set.
  * Encode supports sub in {1, 2, 4, 8} and bits in 1..12; decode attention
- * supports (k_sub, k_bits) in {(2, 8), (4, 8)} and (v_sub, v_bits) in
- * {(2, 8), (4, 8), (4, 9)}.
+ * supports (k_sub, k_bits) in {(2, 8), (4, 8)} with (v_sub, v_bits) in
+ * {(2, 8), (4, 8), (4, 9)}, and the 1.5-bit format (8, 12) with (8, 12)
+ * (VecInfer, 实验结果, codebook-size ablation: 2^12 centroids of 8 elements).
  */
 vq_status vq_check_layout(const vq_layout* layout, int32_t for_decode);
 

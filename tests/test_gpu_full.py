@@ -1,7 +1,7 @@
 """Parity at the workloads' full sizes, in the launch configuration bench.py times.
 
 For each workload (32K, ragged paged batch, 196K with drift, batch-64 GQA-5 with
-9-bit values): the whole cache is encoded on the GPU (prefill plus the appended
+9-bit values, 32K in the 1.5-bit configuration): the whole cache is encoded on the GPU (prefill plus the appended
 token) and decoded with the library's default split count and launch shape.
 The oracle then checks sampled (sequence, KV head) pairs one by one:
   - the codes of all N + 1 tokens: bit-exact except in-band ties (logged);
@@ -23,7 +23,7 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 4])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
 def test_full_size_sampled_parity(cfg):
     w = W.WORKLOADS[cfg]
     cal = stored_calib(cfg)
@@ -37,7 +37,7 @@ def test_full_size_sampled_parity(cfg):
     G = w.num_q_heads // w.num_kv_heads
     rng = np.random.default_rng(4000 + cfg)
     pairs = {(int(rng.integers(w.batch)), int(rng.integers(w.num_kv_heads)))
-             for _ in range(1 if cfg == 3 else 2)}
+             for _ in range(1 if cfg in (3, 5) else 2)}
     pairs.add((w.batch - 1, w.num_kv_heads - 1))
     log, refs, tied = [], {}, {}
     for b, h in sorted(pairs):

@@ -12,7 +12,8 @@ def test_table_matches_workload_shapes():
     assert (w[2].batch, w[2].page_size, w[2].ragged_lo, w[2].ragged_hi) == (16, 64, 4096, 8192)
     assert (w[3].context, w[3].drift) == (196608, True)
     assert (w[4].batch, w[4].num_q_heads, w[4].group, w[4].v_bits) == (64, 40, 5, 9)
-    assert [x.k_code_bytes() + x.v_code_bytes() for x in w.values()] == [96, 64, 96, 64, 100]
+    assert (w[5].k_sub, w[5].k_bits, w[5].v_sub, w[5].v_bits) == (8, 12, 8, 12)
+    assert [x.k_code_bytes() + x.v_code_bytes() for x in w.values()] == [96, 64, 96, 64, 100, 48]
 
 
 def test_kv_tokens_deterministic_and_windowed():

@@ -93,6 +93,10 @@ WORKLOADS: Dict[int, Workload] = {
                 page_size=256, drift=True),
     4: Workload(4, "qwen2.5-14b-b64-n16384", batch=64, num_q_heads=40, num_kv_heads=8,
                 context=16384, k_sub=2, k_bits=8, v_sub=4, v_bits=9, page_size=256),
+    # The pages' 1.5-bit configuration (VecInfer, 实验结果, codebook-size ablation:
+    # 2^12 centroids of 8 elements for 1.5 bits) on the 32K Llama layer.
+    5: Workload(5, "llama3.1-8b-b1-n32768-1.5bit", batch=1, num_q_heads=32, num_kv_heads=8,
+                context=32768, k_sub=8, k_bits=12, v_sub=8, v_bits=12, page_size=256),
 }
 
 
