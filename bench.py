@@ -298,6 +298,66 @@ def fp16_comparison(torch, w, dev, steps, l2):
             "padded_tokens_per_sequence": N}
 
 
+def graph_ms(torch, dev, fn, steps):
+    """Milliseconds per call of fn(i): 3 eager calls, then `steps` calls captured
+    in one CUDA graph, replayed once to warm up and once between events."""
+    for i in range(3):
+        fn(i)
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(gr, stream=s):
+            for i in range(steps):
+                fn(i)
+    torch.cuda.current_stream().wait_stream(s)
+    gr.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    gr.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def residual_comparison(torch, vq, w, layout, pools, lam_d, ck_d, cv_d, q_d, table_d, seq_d,
+                        max_len, num_pages, splits, steps, dev, window=128):
+    """Context: decode attention with the pages' full-precision residual window
+    (实验结果 / 实验设置: 128 tokens) through vq_decode_attention_residual, against
+    vq_decode_attention on the same quantized cache, timed like the step."""
+    B, Hq, Hkv, D = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+    g = torch.Generator(device=dev).manual_seed(0)
+    k_res = torch.randn((B, Hkv, window, D), generator=g, device=dev, dtype=torch.float16)
+    v_res = torch.randn((B, Hkv, window, D), generator=g, device=dev, dtype=torch.float16)
+    res_lens = torch.full((B,), window, dtype=torch.int32, device=dev)
+    ws_bytes = vq.vq_decode_residual_workspace_bytes(layout, B, max_len, splits)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty((B, Hq, D), dtype=torch.float16, device=dev)
+    copies = len(pools)
+    p = lambda t: t.data_ptr()  # noqa: E731
+
+    def plain(i):
+        kp, vp = pools[i % copies]
+        vq.vq_decode_attention(layout, B, p(q_d), p(lam_d), p(ck_d), p(cv_d), p(kp), p(vp), num_pages,
+                               p(table_d), table_d.shape[1], p(seq_d), max_len, 0.0, splits, p(out),
+                               p(ws), ws_bytes, None, torch.cuda.current_stream().cuda_stream)
+
+    def with_window(i):
+        kp, vp = pools[i % copies]
+        vq.vq_decode_attention_residual(layout, B, p(q_d), p(lam_d), p(ck_d), p(cv_d), p(kp), p(vp),
+                                        num_pages, p(table_d), table_d.shape[1], p(seq_d), max_len,
+                                        p(k_res), p(v_res), p(res_lens), window, 0.0, splits, p(out),
+                                        p(ws), ws_bytes, None, torch.cuda.current_stream().cuda_stream)
+
+    plain_ms = graph_ms(torch, dev, plain, steps)
+    window_ms = graph_ms(torch, dev, with_window, steps)
+    return {"window_tokens": window, "attention_us": plain_ms * 1e3,
+            "attention_with_window_us": window_ms * 1e3,
+            "window_overhead_us": (window_ms - plain_ms) * 1e3}
+
+
 def unfused_comparison(torch, vq, w, layout, pools, lam_d, ck_d, cv_d, q_d, num_pages, lens,
                        steps, dev):
     """Context, not the product path: the unfused pipeline VecInfer compares its
@@ -334,29 +394,8 @@ def unfused_comparison(torch, vq, w, layout, pools, lam_d, ck_d, cv_d, q_d, num_
         dequant(i)
         return F.scaled_dot_product_attention(q4, k4, v4, enable_gqa=True)
 
-    def timed(fn):
-        for i in range(3):
-            fn(i)
-        torch.cuda.synchronize()
-        gr = torch.cuda.CUDAGraph()
-        s = torch.cuda.Stream(device=dev)
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            with torch.cuda.graph(gr, stream=s):
-                for i in range(steps):
-                    fn(i)
-        torch.cuda.current_stream().wait_stream(s)
-        gr.replay()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        gr.replay()
-        b.record()
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / steps
-
-    ms = timed(one)
-    dq_ms = timed(dequant)
+    ms = graph_ms(torch, dev, one, steps)
+    dq_ms = graph_ms(torch, dev, dequant, steps)
     code_bytes = B * N * Hkv * (layout_row_bytes(w, "k") + layout_row_bytes(w, "v"))
     del k_hat, v_hat, k4, v4
     torch.cuda.empty_cache()
@@ -651,7 +690,7 @@ def main():
                "h2d_bytes_per_step": q_p.numel() * 2 + k_p.numel() * 2 + v_p.numel() * 2,
                "d2h_bytes_per_step": out_p.numel() * 2, "ms_per_step": e_ms}
 
-    comparison = unfused = None
+    comparison = unfused = residual = None
     if world == 1 and not args.no_fp16_compare:
         try:
             comparison = fp16_comparison(torch, w, dev, min(K, 200), l2)
@@ -668,6 +707,12 @@ def main():
                 unfused["dequantize_hbm_frac"] = unfused["dequantize_gbs"] / hbm_peak
         except Exception as exc:
             unfused = {"skipped": f"{type(exc).__name__}: {exc}"[:200]}
+        try:
+            residual = residual_comparison(torch, vq, w, layout, pools, lam_d, ck_d, cv_d, q_d,
+                                           table_d, seq_d, max_len, num_pages, splits,
+                                           min(K, 200), dev)
+        except Exception as exc:
+            residual = {"skipped": f"{type(exc).__name__}: {exc}"[:200]}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -696,6 +741,7 @@ def main():
             "prefill_encode": encode_report(w, prefill_tokens, enc_ms, sms, clocks),
             "fp16_comparison": comparison,
             "unfused_comparison": unfused,
+            "residual_window": residual,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * K, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
