@@ -116,3 +116,71 @@ def test_empty_calls_are_noops(lib):
     vq.vq_encode_kv(L, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4)
     vq.vq_decode_attention(L, 0, None, None, None, None, None, None, 1, None, 1, None, 0, 0.0, 0,
                            None, None, 0)
+
+
+def test_check_layout_one_and_a_half_bit(lib):
+    L = vq.make_layout(k_sub=8, k_bits=12, v_sub=8, v_bits=12)
+    vq.vq_check_layout(L, True)                      # the pages' 1.5-bit configuration
+    assert vq.vq_code_row_bytes(128, 8, 12) == 24
+    for kw in (dict(k_sub=8, k_bits=12, v_sub=8, v_bits=8), dict(k_sub=8, k_bits=11, v_sub=8, v_bits=12),
+               dict(k_sub=4, k_bits=8, v_sub=8, v_bits=12)):
+        with pytest.raises(vq.VQError) as e:
+            vq.vq_check_layout(vq.make_layout(**kw), True)
+        assert e.value.status == vq.VQ_ERR_UNSUPPORTED, kw
+
+
+def test_residual_workspace_is_the_split_workspace_plus_one_partial_per_row(lib):
+    L = vq.make_layout()
+    n = vq.vq_decode_workspace_bytes(L, 3, 32769, 19, 152)
+    r = vq.vq_decode_residual_workspace_bytes(L, 3, 32769, 19, 152)
+    rows = 3 * 32
+    assert r == n + (rows * 128 * 4 + 255) // 256 * 256 + (rows * 8 + 255) // 256 * 256
+    assert vq.vq_decode_residual_workspace_bytes(L, 3, 32769, 0, 152) == \
+        vq.vq_decode_residual_workspace_bytes(L, 3, 32769, vq.vq_default_num_splits(L, 3, 32769, 152), 152)
+    assert vq.vq_decode_residual_workspace_bytes(L, -1, 10, 0, 152) == 0
+
+
+def test_residual_rejects_bad_arguments(lib):
+    L = vq.make_layout()
+    args = dict(layout=L, batch=1, q=FAKE, lambda_=FAKE, codebook_k=FAKE, codebook_v=FAKE,
+                k_pool=FAKE, v_pool=FAKE, num_pages=4, page_table=FAKE, max_pages_per_seq=4,
+                seq_lens=FAKE, max_seq_len=100, k_res=FAKE, v_res=FAKE, res_lens=FAKE,
+                res_capacity=128, softmax_scale=0.0, num_splits=0, out=FAKE, workspace=FAKE,
+                workspace_bytes=1 << 30)
+    bad = [dict(res_capacity=0), dict(res_capacity=4097), dict(k_res=None), dict(v_res=FAKE + 4),
+           dict(res_lens=None), dict(out=None), dict(batch=-1), dict(q=None)]
+    for kw in bad:
+        with pytest.raises(vq.VQError) as e:
+            vq.vq_decode_attention_residual(**dict(args, **kw))
+        assert e.value.status == vq.VQ_ERR_INVALID_ARG, kw
+    with pytest.raises(vq.VQError) as e:
+        vq.vq_decode_attention_residual(**dict(args, layout=vq.make_layout(v_sub=8)))
+    assert e.value.status == vq.VQ_ERR_UNSUPPORTED
+    vq.vq_decode_attention_residual(**dict(args, batch=0, q=None, k_res=None))  # empty batch: no-op
+
+
+def test_dequantize_rejects_bad_arguments(lib):
+    L = vq.make_layout()
+    args = dict(layout=L, num_tokens=4, slot_mapping=FAKE, lambda_=FAKE, codebook_k=FAKE,
+                codebook_v=FAKE, k_pool=FAKE, v_pool=FAKE, num_pages=4, k_out=FAKE, v_out=FAKE)
+    bad = [dict(num_tokens=-1), dict(k_out=None, v_out=None), dict(slot_mapping=None),
+           dict(num_pages=0), dict(lambda_=None), dict(codebook_v=None), dict(k_pool=None),
+           dict(k_out=FAKE + 8), dict(layout=vq.make_layout(page_size=8))]
+    for kw in bad:
+        with pytest.raises(vq.VQError) as e:
+            vq.vq_dequantize_kv(**dict(args, **kw))
+        assert e.value.status == vq.VQ_ERR_INVALID_ARG, kw
+    vq.vq_dequantize_kv(**dict(args, num_tokens=0, k_out=None, v_out=None))  # no tokens: no-op
+
+
+def test_step_rejects_bad_arguments(lib):
+    L = vq.make_layout()
+    args = dict(layout=L, batch=1, q=FAKE, k_new=FAKE, v_new=FAKE, lambda_=FAKE, codebook_k=FAKE,
+                codebook_v=FAKE, k_pool=FAKE, v_pool=FAKE, num_pages=4, page_table=FAKE,
+                max_pages_per_seq=4, seq_lens=FAKE, max_seq_len=100, softmax_scale=0.0,
+                num_splits=0, out=FAKE, workspace=FAKE, workspace_bytes=1 << 30)
+    for kw in (dict(k_new=None), dict(v_new=FAKE + 2), dict(out=None), dict(batch=-3),
+               dict(page_table=None), dict(num_pages=0)):
+        with pytest.raises(vq.VQError) as e:
+            vq.vq_decode_step(**dict(args, **kw))
+        assert e.value.status == vq.VQ_ERR_INVALID_ARG, kw

@@ -121,9 +121,9 @@ def compare_codes(gpu: np.ndarray, orc: np.ndarray, x: np.ndarray, C: np.ndarray
 
 
 def write_tie_log(name: str, rows: list) -> Optional[str]:
-    """Tie log as CSV under $VQ_TIE_LOG_DIR (default: gpurun_out if present, else none)."""
-    d = os.environ.get("VQ_TIE_LOG_DIR") or ("gpurun_out" if os.path.isdir("gpurun_out") else None)
-    if not d or not rows:
+    """Tie log as CSV under $VQ_TIE_LOG_DIR (default: tests/tie_logs)."""
+    d = os.environ.get("VQ_TIE_LOG_DIR") or os.path.join(os.path.dirname(os.path.abspath(__file__)), "tie_logs")
+    if not rows:
         return None
     os.makedirs(d, exist_ok=True)
     path = os.path.join(d, f"ties_{name}.csv")
