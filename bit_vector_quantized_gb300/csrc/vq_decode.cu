@@ -776,36 +776,60 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   for (int k = 0; k < n_units; ++k) {
     const UnitStages u = unit_stages<kStageTok>(p, k, ulen_c[k]);
     consumer_sync<NW>();  // previous unit's merge buffers and q~ are free
-    if (warp < G) {       // q~ = q diag(lambda) H_D * scale * log2(e)
-      const __half2 lo = *reinterpret_cast<const __half2*>(&q_r.x);
-      const __half2 hi = *reinterpret_cast<const __half2*>(&q_r.y);
-      float x[4] = {__low2float(lo) * lam_r.x, __high2float(lo) * lam_r.y,
-                    __low2float(hi) * lam_r.z, __high2float(hi) * lam_r.w};
-      fwht128_warp(x, lane);
-      reinterpret_cast<float4*>(qt + warp * kHeadDim)[lane] =
-          make_float4(x[0] * p.qscale, x[1] * p.qscale, x[2] * p.qscale, x[3] * p.qscale);
-      load_q(k + 1);  // prefetch the next unit's query
+    // q~ = q diag(lambda) H_D * scale * log2(e), split into fp16 hi + lo parts
+    // and stored in the score mma's B-operand order: table [head][hi, lo][c][16
+    // words], words 2kk, 2kk+1 = dims 32c + 4kk + {0, 1} and {2, 3} (lane l of
+    // the head's warp holds dims 4l .. 4l+3, i.e. c = l / 8, kk = l % 8).  Heads
+    // G .. NG-1 are zeros.  The consumers then read their operands with a few
+    // 16-byte loads: this per-unit code stays short, which matters because it
+    // runs once per unit, out of an instruction cache the stage loop has just
+    // filled.
+    if (warp < NG) {
+      uint32_t h01 = 0u, l01 = 0u, h23 = 0u, l23 = 0u;
+      if (warp < G) {
+        const __half2 lo = *reinterpret_cast<const __half2*>(&q_r.x);
+        const __half2 hi = *reinterpret_cast<const __half2*>(&q_r.y);
+        float x[4] = {__low2float(lo) * lam_r.x, __high2float(lo) * lam_r.y,
+                      __low2float(hi) * lam_r.z, __high2float(hi) * lam_r.w};
+        fwht128_warp(x, lane);
+        split_half2(x[0] * p.qscale, x[1] * p.qscale, h01, l01);
+        split_half2(x[2] * p.qscale, x[3] * p.qscale, h23, l23);
+        load_q(k + 1);  // prefetch the next unit's query
+      }
+      uint32_t* qf = reinterpret_cast<uint32_t*>(qt) + (warp * 2 * 4 + (lane >> 3)) * 16 + 2 * (lane & 7);
+      *reinterpret_cast<uint2*>(qf) = make_uint2(h01, h23);
+      *reinterpret_cast<uint2*>(qf + 4 * 16) = make_uint2(l01, l23);
     }
     consumer_sync<NW>();
     // B operands of the score mma: k-step kk, rows {2c, 2c+1, 2c+8, 2c+9} hold
-    // dims 32c + 4kk + {0, 1, 2, 3}; column = r.
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const int g = NG == 4 ? (r >> 1) : r;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (g < G) v = reinterpret_cast<const float4*>(qt + g * kHeadDim)[8 * c + kk];
-      uint32_t h01, l01, h23, l23;
-      split_half2(v.x, v.y, h01, l01);
-      split_half2(v.z, v.w, h23, l23);
+    // dims 32c + 4kk + {0, 1, 2, 3}; column = r (G <= 4: head r / 2, hi part
+    // for even r, lo for odd r; G > 4: head r, hi in qa and lo in qb).
+    {
+      const uint4* qf = reinterpret_cast<const uint4*>(qt);
       if constexpr (NG == 4) {
-        const bool lo_col = (r & 1) != 0;
-        qa[kk][0] = lo_col ? l01 : h01;
-        qa[kk][1] = lo_col ? l23 : h23;
+        const int blk = ((r >> 1) * 2 + (r & 1)) * 4 + c;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 wv = qf[blk * 4 + i];
+          qa[2 * i][0] = wv.x;
+          qa[2 * i][1] = wv.y;
+          qa[2 * i + 1][0] = wv.z;
+          qa[2 * i + 1][1] = wv.w;
+        }
       } else {
-        qa[kk][0] = h01;
-        qa[kk][1] = h23;
-        qb[kk][0] = l01;
-        qb[kk][1] = l23;
+        const int bh = (r * 2) * 4 + c, bl = (r * 2 + 1) * 4 + c;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 wh = qf[bh * 4 + i], wl = qf[bl * 4 + i];
+          qa[2 * i][0] = wh.x;
+          qa[2 * i][1] = wh.y;
+          qa[2 * i + 1][0] = wh.z;
+          qa[2 * i + 1][1] = wh.w;
+          qb[2 * i][0] = wl.x;
+          qb[2 * i][1] = wl.y;
+          qb[2 * i + 1][0] = wl.z;
+          qb[2 * i + 1][1] = wl.w;
+        }
       }
     }
 #pragma unroll

@@ -127,7 +127,7 @@ __host__ __device__ inline DecodeSmem decode_smem(int k_bits, int v_bits, int gr
   int o = 0;
   const int rows = 1 << (k_bits > v_bits ? k_bits : v_bits);
   s.tab = o; o = align128(o + rows * (k_bits == 12 ? kTabRowWide : kTabRow));
-  s.qt = o; o = align128(o + group * 128 * 4);
+  s.qt = o; o = align128(o + (group > 4 ? 8 : 4) * 128 * 4);  // q~ operand table, 4 or 8 heads
   s.merge = o; o = align128(o + warps * group * 128 * 4);
   s.ml = o; o = align128(o + warps * group * 8);
   s.units = o; o = align128(o + 2 * kMaxUnitsPerCta * 4);  // consumer and producer copies
