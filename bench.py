@@ -30,6 +30,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -49,7 +50,8 @@ UNIT = "KV tokens/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 CALIB_DIR = os.path.join(ROOT, "tests", "golden", "calib")
-KERNEL_SRC = os.path.join(ROOT, "bit_vector_quantized_gb300", "csrc", "vq_decode.cu")
+KERNEL_SRCS = [os.path.join(ROOT, "bit_vector_quantized_gb300", "csrc", f)
+               for f in ("vq_decode.cu", "vq_device.cuh", "vq_kernels.h")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
 
 
@@ -93,8 +95,16 @@ def measured_hbm():
 
 
 def kernel_hash():
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256[:16] of the split kernel's code: its source file and the headers it
+    includes, without comments and blank lines (an edited comment keeps a traffic
+    record; any code change drops it)."""
+    lines = []
+    for path in KERNEL_SRCS:
+        with open(path) as f:
+            text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        lines += [ln.rstrip() for ln in text.splitlines() if ln.strip()]
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
 
 
 def recorded_traffic(workload):

@@ -12,38 +12,45 @@
 // with the same recurrence.
 //
 // How it maps to GB300:
-//   * Work unit = (sequence, KV head, split).  A persistent grid of one
-//     8-warp CTA per SM walks its units; each warp walks a contiguous run of
-//     16-token chunks inside each unit.  All G query heads of the KV head are
-//     served by the same CTA, so every code byte is read from HBM once.
-//     Split boundaries depend on max_seq_len only, so the page-table prefetch
-//     never waits for seq_lens; chunks past a sequence's end are skipped.
-//   * Code chunks stream HBM -> shared memory with the TMA bulk-copy engine
-//     (cp.async.bulk, completion on an mbarrier): a private ring of `nstage`
-//     chunk slots per warp, refilled as soon as slots free (VecInfer,
-//     "异步流水线执行": asynchronous prefetch of the next block).  Page numbers
-//     come from a double-buffered 32-entry window per warp, loaded by all lanes
-//     in parallel 32 chunks ahead of use.
-//   * Dequantisation is a gather of fp16 centroids straight into warp-mma
+//   * Work unit = (sequence, KV head, split).  A persistent grid of at most one
+//     CTA per SM walks its units.  A CTA has NW consumer warps (12 for G <= 4,
+//     8 for G > 4) and 4 producer warps, and serves all G query heads of the
+//     unit's KV head, so every code byte is read from HBM once.  Split
+//     boundaries are 32-token blocks of max_seq_len; a unit covers its blocks
+//     up to the sequence's length.
+//   * Pipeline stages of NW x 16 tokens (their K rows, then their V rows)
+//     stream HBM -> shared memory with the TMA bulk-copy engine (cp.async.bulk,
+//     completion on the stage slot's "full" mbarrier) into a ring of `nstage`
+//     slots, released by the consumers through "empty" mbarriers (VecInfer,
+//     "异步流水线执行": asynchronous prefetch of the next blocks).  Producer warp
+//     w issues stages w, w + 4, ...: each lane copies one piece (at most 4 KB,
+//     never crossing a page) after looking up its page 4 stages ahead, so
+//     several warps keep enough bytes in flight.
+//   * Consumer warp w takes the w-th 16-token chunk of every stage.
+//     Dequantisation is a gather of fp16 centroids straight into warp-mma
 //     operand registers.  Codebooks stay resident in shared memory, replicated
 //     16x (8-byte centroids) or 32x (4-byte centroids); lane L reads copy L % 16
 //     (L), which places every lane's gather in its own bank pair (bank): gathers
-//     are free of bank conflicts whatever the codes.
+//     are free of bank conflicts whatever the codes.  The 1.5-bit format (4096
+//     centroids of 8 elements) cannot be replicated and uses a half-major table.
 //   * Both contractions run on the tensor pipe with m16n8k16 fp16 mma, fp32
 //     accumulation.  Scores: s^T[16 tok x 8] = K^[16 tok x 128] q~^T; values:
-//     o^T[128 x 8] += V^^T[128 x 16 tok] P^T[16 tok x 8].  Because q~ and p are
-//     rounded to fp16 operands, each is split into hi + lo fp16 parts: with
-//     G <= 4 the hi and lo parts occupy the otherwise empty columns 2g and 2g+1
-//     of the 8-wide operand (no extra mma); with 4 < G <= 8 hi and lo take one
-//     mma each.  Centroids are exact fp16 values, so the products keep about
-//     fp32 accuracy.
+//     o^T[128 x 8] += V^^T[128 x 16 tok] P^T[16 tok x 8].  q~ is split into
+//     fp16 hi + lo parts, so the scores keep about fp32 accuracy: with G <= 4
+//     the hi and lo parts occupy the otherwise empty columns 2g and 2g+1 of the
+//     8-wide operand (no extra mma); with 4 < G <= 8 hi and lo take one mma
+//     each.  Centroids are exact fp16 values; p (at most 2^8 with the lazy
+//     running maximum) is rounded to fp16 once.
 //   * The K and V feature dimensions are permuted consistently (a dot product
 //     and an output row set do not depend on the order) so that each lane's
 //     operand registers are exactly one centroid gather: the lane with
 //     (lane % 4) = c holds dims 32c + 4k .. 32c + 4k + 3 of k-step k for K, and
 //     the lane with lane / 4 = r accumulates output dims 16r .. 16r + 15 for V.
-//   * Each warp iteration processes two 16-token chunks, so the two mma chains,
-//     their gathers and the softmax bookkeeping overlap.
+//   * Each stage's scores and the previous stage's P.V form one basic block, so
+//     the two mma chains, their gathers and the softmax bookkeeping overlap.
+//   * Every mbarrier wait is bounded (%globaltimer); on a timeout the CTA
+//     raises an abort flag, drains its copies in flight and reports
+//     VQ_DEV_TIMEOUT.  Launch ordering follows pdl_wait in vq_device.cuh.
 #include <type_traits>
 
 #include "vq_device.cuh"
