@@ -11,11 +11,15 @@
 // (2 in registers, 5 by shuffle), scale by 1/sqrt(128).  Each lane then owns
 // the sub-vectors covering its 4 elements and scans the codebook, which the
 // CTA keeps in shared memory as (-2 c_j, ||c_j||^2) in fp32: the score
-// ||c_j||^2 - 2 x.c_j orders centroids exactly as ||x - c_j||^2 does.  All
-// lanes read the same centroid at once (a shared-memory broadcast), so the
-// scan is bound by the FP32 pipe.  With few tokens (a decode-step append) the
-// scan of one vector is split over `split` warps that each take a slice of the
-// codebook, and the slices are merged keeping the lowest index on ties.
+// ||c_j||^2 - 2 x.c_j orders centroids exactly as ||x - c_j||^2 does.  The
+// lanes read one or two centroids at once (shared-memory broadcasts), so the
+// scan is bound by the FP32 pipe.  For d = 8 the two lanes that share a
+// sub-vector each form its whole dot product and take alternate centroids;
+// for d <= 4, four centroids per iteration keep several FMA chains in flight.
+// Many vectors with d = 2 or 4 (a prefill) go four to a warp, sharing every
+// centroid load.  With few tokens (a decode-step append) the scan of one
+// vector is split over `split` warps that each take a slice of the codebook,
+// and the slices are merged keeping the lowest index on ties.
 // Finally the warp packs the codes into the LSB-first bit stream of the row
 // (one 32-bit word per lane) and stores it into the token's paged slot.
 #include "vq_device.cuh"
