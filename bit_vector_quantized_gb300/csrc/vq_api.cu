@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -36,19 +37,27 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
-int device_sms() {
+// Device attributes the launch choices need, read once per device.
+struct DeviceAttrs {
+  std::atomic<int> sms[vqk::kMaxDevices] = {};
+  std::atomic<int> smem_optin[vqk::kMaxDevices] = {};
+};
+DeviceAttrs g_attrs;
+
+int device_attr(std::atomic<int>* cache, cudaDeviceAttr attr) {
   int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= vqk::kMaxDevices) return 0;
+  n = cache[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, attr, dev) != cudaSuccess) return 0;
+  cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
+int device_sms() { return device_attr(g_attrs.sms, cudaDevAttrMultiProcessorCount); }
+
 int device_smem_optin() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-    return 0;
-  return n;
+  return device_attr(g_attrs.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin);
 }
 
 bool decode_formats_supported(const vq_layout& L) {
@@ -144,7 +153,8 @@ vq_status vq_check_layout(const vq_layout* layout, int32_t for_decode) {
 // codebooks, pools, lambda, the slot source and the status word; the launch
 // shape follows from the number of vectors.
 vq_status launch_encode_impl(const vq_layout& L, vqk::EncodeParams& p, int32_t num_tokens,
-                             bool has_k, bool has_v, void* stream, const char* what) {
+                             bool has_k, bool has_v, void* stream, const char* what,
+                             bool overlap) {
   p.sub[0] = L.k_sub;
   p.sub[1] = L.v_sub;
   p.bits[0] = L.k_bits;
@@ -173,7 +183,7 @@ vq_status launch_encode_impl(const vq_layout& L, vqk::EncodeParams& p, int32_t n
   if (optin > 0 && smem > static_cast<size_t>(optin))
     return fail(VQ_ERR_UNSUPPORTED, "encode needs %zu bytes of shared memory, device has %d", smem, optin);
   cudaError_t e = vqk::launch_encode(p, static_cast<int>(grid_x), grid_y, smem,
-                                     static_cast<cudaStream_t>(stream));
+                                     static_cast<cudaStream_t>(stream), overlap);
   if (e != cudaSuccess) return cuda_fail(e, what);
   return VQ_OK;
 }
@@ -210,7 +220,7 @@ vq_status vq_encode_kv(const vq_layout* layout, int32_t num_tokens, const void* 
   p.status = status;
   p.num_slots = static_cast<long long>(num_pages) * L.page_size;
   return launch_encode_impl(L, p, num_tokens, k != nullptr, v != nullptr, stream,
-                            "vq_encode_kv launch");
+                            "vq_encode_kv launch", false);
 }
 
 vq_status vq_dequantize_kv(const vq_layout* layout, int32_t num_tokens,
@@ -398,9 +408,9 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
 // CTAs of the decode step's append encode: one warp per (sequence, KV head)
 // vector, 8 per CTA, keys and values.
 vq_status launch_partial(const vq_layout& L, const vqk::DecodeParams& p, int grid, size_t smem,
-                         void* stream) {
+                         void* stream, bool overlap) {
   cudaError_t e = vqk::launch_decode(p, L.k_sub, L.k_bits, L.v_sub, L.v_bits, grid, smem,
-                                     static_cast<cudaStream_t>(stream));
+                                     static_cast<cudaStream_t>(stream), overlap);
   if (e != cudaSuccess) return cuda_fail(e, "decode split kernel");
   return VQ_OK;
 }
@@ -421,7 +431,7 @@ ResLayout res_layout(const vq_layout& L, int batch, int splits) {
 
 vq_status combine_impl(const vq_layout* layout, int32_t batch, int32_t max_seq_len,
                        int32_t num_splits, const void* workspace, size_t workspace_bytes,
-                       void* out, void* stream, bool residual = false) {
+                       void* out, void* stream, bool overlap, bool residual = false) {
   const vq_layout& L = *layout;
   if (!workspace || !out) return fail(VQ_ERR_INVALID_ARG, "workspace or out is NULL");
   if (!aligned16(workspace) || !aligned16(out))
@@ -450,7 +460,7 @@ vq_status combine_impl(const vq_layout* layout, int32_t batch, int32_t max_seq_l
   cp.out = out;
   cp.rows = batch * L.num_q_heads;
   cp.splits = splits;
-  cudaError_t e = vqk::launch_combine(cp, static_cast<cudaStream_t>(stream));
+  cudaError_t e = vqk::launch_combine(cp, static_cast<cudaStream_t>(stream), overlap);
   if (e != cudaSuccess) return cuda_fail(e, "decode combine kernel");
   return VQ_OK;
 }
@@ -477,7 +487,7 @@ vq_status vq_decode_partial(const vq_layout* layout, int32_t batch, const void* 
                       page_table, max_pages_per_seq, seq_lens, max_seq_len, softmax_scale,
                       num_splits, workspace, workspace_bytes, status, p, grid, smem);
   if (st != VQ_OK) return st;
-  return launch_partial(*layout, p, grid, smem, stream);
+  return launch_partial(*layout, p, grid, smem, stream, false);
 }
 
 vq_status vq_decode_combine(const vq_layout* layout, int32_t batch, int32_t max_seq_len,
@@ -487,7 +497,8 @@ vq_status vq_decode_combine(const vq_layout* layout, int32_t batch, int32_t max_
   if (st != VQ_OK) return st;
   if (batch < 0 || max_seq_len < 0) return fail(VQ_ERR_INVALID_ARG, "batch or max_seq_len < 0");
   if (batch == 0) return VQ_OK;
-  return combine_impl(layout, batch, max_seq_len, num_splits, workspace, workspace_bytes, out, stream);
+  return combine_impl(layout, batch, max_seq_len, num_splits, workspace, workspace_bytes, out, stream,
+                      false);
 }
 
 vq_status vq_decode_step(const vq_layout* layout, int32_t batch, const void* q, const void* k_new,
@@ -531,12 +542,13 @@ vq_status vq_decode_step(const vq_layout* layout, int32_t batch, const void* q, 
   ep.max_pages = max_pages_per_seq;
   ep.status = status;
   ep.num_slots = static_cast<long long>(num_pages) * L.page_size;
-  st = launch_encode_impl(L, ep, batch, true, true, stream, "vq_decode_step append encode");
+  st = launch_encode_impl(L, ep, batch, true, true, stream, "vq_decode_step append encode", false);
   if (st != VQ_OK) return st;
   // 2. split attention (its copies wait for the append), 3. merge of the splits
-  st = launch_partial(L, p, grid, smem, stream);
+  st = launch_partial(L, p, grid, smem, stream, true);
   if (st != VQ_OK) return st;
-  return combine_impl(layout, batch, max_seq_len, p.splits, workspace, workspace_bytes, out, stream);
+  return combine_impl(layout, batch, max_seq_len, p.splits, workspace, workspace_bytes, out, stream,
+                      true);
 }
 
 vq_status vq_decode_attention(const vq_layout* layout, int32_t batch, const void* q,
@@ -559,9 +571,10 @@ vq_status vq_decode_attention(const vq_layout* layout, int32_t batch, const void
                       page_table, max_pages_per_seq, seq_lens, max_seq_len, softmax_scale,
                       num_splits, workspace, workspace_bytes, status, p, grid, smem);
   if (st != VQ_OK) return st;
-  st = launch_partial(*layout, p, grid, smem, stream);
+  st = launch_partial(*layout, p, grid, smem, stream, false);
   if (st != VQ_OK) return st;
-  return combine_impl(layout, batch, max_seq_len, p.splits, workspace, workspace_bytes, out, stream);
+  return combine_impl(layout, batch, max_seq_len, p.splits, workspace, workspace_bytes, out, stream,
+                      true);
 }
 
 }  // extern "C"
@@ -579,25 +592,56 @@ namespace {
 constexpr size_t kStaticScratchBytes = size_t(4) << 20;  // 4 MiB
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchAddr {
+  unsigned long long ctx_id;  // the context the address belongs to (0: not looked up)
+  void* ptr;
+};
+ScratchAddr g_scratch[vqk::kMaxDevices] = {};
 
-// Device address of the array on the current device (a host-side name of a
-// __device__ variable is not a device address); looked up once per device.
+// Identity of the current context, so that an address looked up in a context
+// that has since been destroyed (cudaDeviceReset) is looked up again.  The
+// driver entry points come through the runtime, so no driver library is linked.
+unsigned long long current_context_id() {
+  using GetCurrent = int (*)(void**);
+  using GetId = int (*)(void*, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, nullptr) ==
+        cudaSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, nullptr) ==
+        cudaSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+  });
+  void* ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != 0 || !ctx || get_id(ctx, &id) != 0) return 1;
+  return id + 1;  // never 0
+}
+
+// Device address of the array in the current context (a host-side name of a
+// __device__ variable is not a device address); looked up once per device and
+// context.
 vq_status static_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kMaxDevices) return fail(VQ_ERR_UNSUPPORTED, "device %d out of range", dev);
+  if (dev < 0 || dev >= vqk::kMaxDevices) return fail(VQ_ERR_UNSUPPORTED, "device %d out of range", dev);
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (g_scratch[dev].ctx_id != ctx || !g_scratch[dev].ptr) {
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_static_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
-    g_scratch_ptr[dev] = ptr;
+    g_scratch[dev].ptr = ptr;
+    g_scratch[dev].ctx_id = ctx;
   }
-  *out = g_scratch_ptr[dev];
+  *out = g_scratch[dev].ptr;
   return VQ_OK;
 }
 
@@ -623,9 +667,11 @@ vq_status vq_decode_attention_static(const vq_layout* layout, int32_t batch, con
   if (num_splits > kMaxSplits) return fail(VQ_ERR_INVALID_ARG, "num_splits %d > %d", num_splits, kMaxSplits);
   int splits = num_splits;
   if (splits <= 0) {
+    // the library's split choice, lowered until the partials fit the array
     const int sms = device_sms();
     if (sms <= 0) return fail(VQ_ERR_CUDA, "no CUDA device");
     splits = pick_splits(*layout, batch, max_seq_len, sms);
+    while (splits > 1 && ws_layout(*layout, batch, splits).total > kStaticScratchBytes) --splits;
   }
   const size_t need = ws_layout(*layout, batch, splits).total;
   if (need > kStaticScratchBytes)
@@ -645,9 +691,10 @@ vq_status vq_decode_attention_static(const vq_layout* layout, int32_t batch, con
                       page_table, max_pages_per_seq, seq_lens, max_seq_len, softmax_scale, splits,
                       scratch, kStaticScratchBytes, status, p, grid, smem);
   if (st != VQ_OK) return st;
-  st = launch_partial(*layout, p, grid, smem, stream);
+  st = launch_partial(*layout, p, grid, smem, stream, false);
   if (st != VQ_OK) return st;
-  return combine_impl(layout, batch, max_seq_len, splits, scratch, kStaticScratchBytes, out, stream);
+  return combine_impl(layout, batch, max_seq_len, splits, scratch, kStaticScratchBytes, out, stream,
+                      true);
 }
 
 size_t vq_static_scratch_bytes(void) { return kStaticScratchBytes; }
@@ -718,12 +765,13 @@ vq_status vq_decode_attention_residual(const vq_layout* layout, int32_t batch, c
   rp.capacity = res_capacity;
   const long long rgrid = static_cast<long long>(batch) * L.num_kv_heads;
   if (rgrid > 0x7fffffffLL) return fail(VQ_ERR_INVALID_ARG, "batch %d too large", batch);
-  cudaError_t e = vqk::launch_residual(rp, static_cast<int>(rgrid), static_cast<cudaStream_t>(stream));
+  cudaError_t e = vqk::launch_residual(rp, static_cast<int>(rgrid), static_cast<cudaStream_t>(stream),
+                                       false);
   if (e != cudaSuccess) return cuda_fail(e, "residual attention kernel");
-  st = launch_partial(L, p, grid, smem, stream);
+  st = launch_partial(L, p, grid, smem, stream, true);
   if (st != VQ_OK) return st;
   return combine_impl(layout, batch, max_seq_len, p.splits, workspace, workspace_bytes, out, stream,
-                      true);
+                      true, true);
 }
 
 }  // extern "C"

@@ -65,13 +65,13 @@ __global__ void __launch_bounds__(kHeadDim) vq_combine_kernel(const CombineParam
 
 }  // namespace
 
-cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool overlap) {
   if (p.rows == 0) return cudaSuccess;
   // chunk of partials loaded at once: the smallest of 4, 8, 16, 32 that holds them all
   const int terms = p.splits + (p.res_ml ? 1 : 0);
   auto kern = terms <= 4 ? vq_combine_kernel<4> : terms <= 8 ? vq_combine_kernel<8>
             : terms <= 16 ? vq_combine_kernel<16> : vq_combine_kernel<32>;
-  cudaError_t e = launch_pdl(kern, dim3(p.rows), dim3(kHeadDim), 0, stream, p);
+  cudaError_t e = launch_pdl(kern, dim3(p.rows), dim3(kHeadDim), 0, stream, p, overlap);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

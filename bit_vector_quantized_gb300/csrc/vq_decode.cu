@@ -939,49 +939,39 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   __syncthreads();  // matches the producers' final barrier
 }
 
-template <typename K>
-cudaError_t configure(K kern, size_t smem) {
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                              cudaSharedmemCarveoutMaxShared);
-}
-
 template <int DK, int BK, int DV, int BV, int NG, int NW, int NCH>
-cudaError_t launch_split(const DecodeParams& p, int grid, size_t smem, cudaStream_t stream) {
+cudaError_t launch_split(const DecodeParams& p, int grid, size_t smem, cudaStream_t stream,
+                         bool overlap) {
   auto kern = vq_decode_split_kernel<DK, BK, DV, BV, NG, NW, NCH>;
-  static size_t configured = 0;
-  if (smem > configured) {
-    cudaError_t e = configure(kern, smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
-  cudaError_t e = launch_pdl(kern, dim3(grid), dim3((NW + kProducerWarps) * 32), smem, stream, p);
+  static SmemOptIn opt_in;
+  cudaError_t e = ensure_smem(kern, smem, opt_in);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(kern, dim3(grid), dim3((NW + kProducerWarps) * 32), smem, stream, p, overlap);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int DK, int BK, int DV, int BV>
-cudaError_t launch_formats(const DecodeParams& p, int grid, size_t smem, cudaStream_t stream) {
+cudaError_t launch_formats(const DecodeParams& p, int grid, size_t smem, cudaStream_t stream,
+                           bool ov) {
   const bool wide = p.group > 4;
   if (p.warps == 12 && p.chunks == 1)
-    return wide ? launch_split<DK, BK, DV, BV, 8, 12, 1>(p, grid, smem, stream)
-                : launch_split<DK, BK, DV, BV, 4, 12, 1>(p, grid, smem, stream);
+    return wide ? launch_split<DK, BK, DV, BV, 8, 12, 1>(p, grid, smem, stream, ov)
+                : launch_split<DK, BK, DV, BV, 4, 12, 1>(p, grid, smem, stream, ov);
   if (p.warps == 8 && p.chunks == 2)
-    return wide ? launch_split<DK, BK, DV, BV, 8, 8, 2>(p, grid, smem, stream)
-                : launch_split<DK, BK, DV, BV, 4, 8, 2>(p, grid, smem, stream);
+    return wide ? launch_split<DK, BK, DV, BV, 8, 8, 2>(p, grid, smem, stream, ov)
+                : launch_split<DK, BK, DV, BV, 4, 8, 2>(p, grid, smem, stream, ov);
   if (p.warps == 8 && p.chunks == 1)
-    return wide ? launch_split<DK, BK, DV, BV, 8, 8, 1>(p, grid, smem, stream)
-                : launch_split<DK, BK, DV, BV, 4, 8, 1>(p, grid, smem, stream);
+    return wide ? launch_split<DK, BK, DV, BV, 8, 8, 1>(p, grid, smem, stream, ov)
+                : launch_split<DK, BK, DV, BV, 4, 8, 1>(p, grid, smem, stream, ov);
   return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, int k_sub, int k_bits, int v_sub, int v_bits,
-                          int grid, size_t smem, cudaStream_t stream) {
+                          int grid, size_t smem, cudaStream_t stream, bool overlap) {
 #define VQ_CASE(DK, BK, DV, BV) \
-  if (k_sub == DK && k_bits == BK && v_sub == DV && v_bits == BV) return launch_formats<DK, BK, DV, BV>(p, grid, smem, stream);
+  if (k_sub == DK && k_bits == BK && v_sub == DV && v_bits == BV) return launch_formats<DK, BK, DV, BV>(p, grid, smem, stream, overlap);
   VQ_CASE(2, 8, 4, 8)
   VQ_CASE(4, 8, 4, 8)
   VQ_CASE(2, 8, 4, 9)

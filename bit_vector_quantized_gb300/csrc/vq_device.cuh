@@ -26,14 +26,16 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 }
 
 // ------------------------------------------- programmatic dependent launch ---
-// The library's kernels are launched with programmatic stream serialization:
-// a kernel may be scheduled while the previous kernel in the stream still runs
-// if that kernel signals pdl_trigger, which only the library's own kernels do.
-// Those write nothing but code pools, workspaces, outputs and status words, so
-// before pdl_wait a kernel reads only inputs that are none of these
-// (codebooks, lambda, queries, new keys/values, page tables, lengths, slots)
-// and writes nothing; pdl_wait blocks until the previous kernel has completed
-// and its memory is visible.  Without the launch attribute both are no-ops.
+// A kernel launched with programmatic stream serialization may be scheduled
+// while the previous kernel in the stream still runs, once that kernel
+// signals pdl_trigger.  The library launches only the second and later
+// kernels of one call that way, and the first kernel of a call starts after
+// all earlier stream work has completed; so before pdl_wait a kernel reads
+// only its call's inputs that the previous kernel of the same call does not
+// write (codebooks, lambda, queries, new keys/values, page tables, lengths,
+// slots) and writes nothing.  pdl_wait blocks until the previous kernel has
+// completed and its memory is visible.  Without the launch attribute both
+// are no-ops.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -498,19 +498,11 @@ size_t encode_smem_bytes(int sub, int bits) {
 }
 
 cudaError_t launch_encode(const EncodeParams& p, int grid_x, int grid_y, size_t smem,
-                          cudaStream_t stream) {
-  static size_t configured = 0;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(vq_encode_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(vq_encode_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                               cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
-  cudaError_t e = launch_pdl(vq_encode_kernel, dim3(grid_x, grid_y), dim3(kEncWarps * 32), smem, stream, p);
+                          cudaStream_t stream, bool overlap) {
+  static SmemOptIn opt_in;
+  cudaError_t e = ensure_smem(vq_encode_kernel, smem, opt_in);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(vq_encode_kernel, dim3(grid_x, grid_y), dim3(kEncWarps * 32), smem, stream, p, overlap);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -5,6 +5,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 namespace vqk {
 
 struct EncodeParams {
@@ -139,11 +142,17 @@ __host__ __device__ inline DecodeSmem decode_smem(int k_bits, int v_bits, int gr
   return s;
 }
 
-// Launches `kern` with programmatic stream serialization (see pdl_wait in
-// vq_device.cuh).
+// Launches `kern`.  With `overlap` the launch carries programmatic stream
+// serialization: the kernel may start while the previous kernel in the stream
+// still runs, once that kernel has signalled pdl_trigger (see pdl_wait in
+// vq_device.cuh).  Without it the kernel starts after all earlier work in the
+// stream has completed.  The first kernel of every public call is launched
+// without `overlap`, so nothing a caller's kernel writes can be read early;
+// only the later kernels of the same call overlap their predecessor, whose
+// early start already followed the completion of everything before the call.
 template <typename Params>
 inline cudaError_t launch_pdl(void (*kern)(Params), dim3 grid, dim3 block, size_t smem,
-                              cudaStream_t stream, const Params& p) {
+                              cudaStream_t stream, const Params& p, bool overlap) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -153,21 +162,50 @@ inline cudaError_t launch_pdl(void (*kern)(Params), dim3 grid, dim3 block, size_
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = overlap ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+constexpr int kMaxDevices = 64;
+
+// The dynamic shared-memory size one kernel has been opted in to, per device
+// (cudaFuncSetAttribute acts on the current device only).
+struct SmemOptIn {
+  std::mutex mu;
+  std::atomic<size_t> bytes[kMaxDevices] = {};
+};
+
+// Raises `kern`'s dynamic shared-memory limit on the current device to at
+// least `smem` bytes and prefers the largest shared-memory carveout, once per
+// device and size.  Thread-safe.
+template <typename K>
+inline cudaError_t ensure_smem(K kern, size_t smem, SmemOptIn& st) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (smem <= st.bytes[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(st.mu);
+  if (smem <= st.bytes[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess) st.bytes[dev].store(smem, std::memory_order_release);
+  return e;
 }
 
 // Launchers (return the cudaError_t of the launch).
 cudaError_t launch_encode(const EncodeParams& p, int grid_x, int grid_y, size_t smem,
-                          cudaStream_t stream);
+                          cudaStream_t stream, bool overlap);
 size_t encode_smem_bytes(int sub, int bits);
 
 // Returns cudaErrorInvalidValue when no kernel is compiled for the formats.
 cudaError_t launch_decode(const DecodeParams& p, int k_sub, int k_bits, int v_sub, int v_bits,
-                          int grid, size_t smem, cudaStream_t stream);
-cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+                          int grid, size_t smem, cudaStream_t stream, bool overlap);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool overlap);
 cudaError_t launch_dequant(const DequantParams& p, int grid_x, cudaStream_t stream);
-cudaError_t launch_residual(const ResidualParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_residual(const ResidualParams& p, int grid, cudaStream_t stream, bool overlap);
 size_t residual_smem_bytes(int group, int capacity);
 int dequant_tokens_per_cta();
 

@@ -170,16 +170,12 @@ size_t residual_smem_bytes(int group, int capacity) {
           static_cast<size_t>(kResWarps) * group * kHeadDim) * sizeof(float);
 }
 
-cudaError_t launch_residual(const ResidualParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_residual(const ResidualParams& p, int grid, cudaStream_t stream, bool overlap) {
   const size_t smem = residual_smem_bytes(p.group, p.capacity);
-  static size_t configured = 0;
-  if (smem > 48 * 1024 && smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(vq_residual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
-  cudaError_t e = launch_pdl(vq_residual_kernel, dim3(grid), dim3(kResThreads), smem, stream, p);
+  static SmemOptIn opt_in;
+  cudaError_t e = ensure_smem(vq_residual_kernel, smem, opt_in);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(vq_residual_kernel, dim3(grid), dim3(kResThreads), smem, stream, p, overlap);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

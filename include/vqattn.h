@@ -18,13 +18,17 @@
  *   - Every call is asynchronous and ordered on the CUDA stream `stream`
  *     (a cudaStream_t passed as void*; NULL = the legacy default stream).
  *     No call synchronises the device.
- *   - Kernels are launched with programmatic stream serialization.  When the
- *     previous kernel in the stream is one of this library's, a kernel may
- *     start before it has finished and read its inputs that are not pools,
- *     workspaces, outputs or status words (codebooks, lambda, queries, new
- *     keys/values, page tables, lengths, slots); it reads no pool and writes
- *     nothing until that kernel has completed.  Those inputs must therefore
- *     not alias a pool, workspace, output or status word of an earlier call.
+ *   - The first kernel of every call starts after all earlier work on
+ *     `stream` has completed, as with any plain launch, so the call sees
+ *     everything the caller wrote before it.  Later kernels of the same call
+ *     (the attention kernel after the append of vq_decode_step, the merge
+ *     after the attention kernel) are launched with programmatic stream
+ *     serialization: each may start while its predecessor in the call runs,
+ *     reading only the call's inputs early, and reads what its predecessor
+ *     writes only after that kernel has completed.  A caller's kernel
+ *     launched after a call with programmatic serialization must wait
+ *     (griddepcontrol.wait / cudaGridDependencySynchronize) before it reads
+ *     the call's outputs, as the CUDA programming model requires.
  *   - Arguments are validated on the host before anything is launched; a
  *     failed check returns a negative vq_status and launches nothing.
  *     vq_last_error() then describes the failure (thread-local string).
@@ -328,12 +332,15 @@ vq_status vq_decode_attention_residual(const vq_layout* layout, int32_t batch, c
  * instead, so it allocates nothing (no cudaMalloc, no cudaFree, no allocating
  * library call).
  *   - The array holds vq_static_scratch_bytes() bytes (4 MiB) on every GPU
- *     that loads the library, until the process exits.  A request whose
- *     vq_decode_workspace_bytes() exceeds that returns VQ_ERR_WORKSPACE and
- *     launches nothing.
+ *     that loads the library, until the process exits.  With num_splits <= 0
+ *     the library's split choice is lowered until the partials fit; a request
+ *     that does not fit even so (or an explicit num_splits whose
+ *     vq_decode_workspace_bytes() exceeds the array) returns
+ *     VQ_ERR_WORKSPACE and launches nothing.
  *   - The first call on a device looks the array's device address up with
- *     cudaGetSymbolAddress (once per device, for the device that is current);
- *     make that first call before any stream capture.
+ *     cudaGetSymbolAddress (once per device and CUDA context, for the device
+ *     that is current); make that first call before any stream capture, and
+ *     again after a cudaDeviceReset.
  *   - All calls on a device share the one array, which keeps the contents of
  *     the last call.  Nothing in it has to start at zero: the split kernel
  *     writes every partial the combine reads.  Calls whose kernels overlap on

@@ -17,7 +17,7 @@ import pytest
 
 import workloads as W
 from vqcase import (GpuCache, check_outputs, compare_codes, oracle_attention, oracle_encode,
-                    stored_calib, write_tie_log)
+                    skip_end_to_end, stored_calib, write_tie_log)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -57,3 +57,54 @@ def test_full_size_sampled_parity(cfg):
         check_outputs(again[b, rows], ref, f"cfg{cfg} b{b} kv-head {h}, oracle codes")
         if tied[(b, h)] == 0:
             check_outputs(got[b, rows], ref, f"cfg{cfg} b{b} kv-head {h}, end to end")
+        else:
+            skip_end_to_end(f"cfg{cfg} b{b} kv-head {h}", tied[(b, h)])
+
+
+def test_full_size_codes_exhaustive_llama_32k():
+    """Every code of the 32K workload (8 KV heads x 32769 tokens, K and V)
+    against the oracle: bit-exact except in-band ties."""
+    w = W.WORKLOADS[1]
+    cal = stored_calib(1)
+    gc = GpuCache(w, cal)
+    gc.prefill()
+    gc.append()
+    assert gc.device_status() == 0
+    n = int(gc.lens[0]) + 1
+    log = []
+    r = oracle_encode(w, cal, 0, 0, n)
+    kc, vc = gc.codes(0, 0, n)
+    compare_codes(kc, r.kc, r.kx, cal.ck, w.k_sub, "cfg1/k/all", log)
+    compare_codes(vc, r.vc, r.vx, cal.cv, w.v_sub, "cfg1/v/all", log)
+    write_tie_log("full_cfg1_all", log)
+
+
+def test_full_size_decode_step_default_splits_llama_32k():
+    """The call bench.py times, vq_decode_step with the library's split count,
+    at the 32K workload's full size: every query head against the oracle.
+
+    The cached 32768 tokens hold the oracle's own codes (written into the
+    pools); the step encodes and appends token 32768 itself, so its codes are
+    compared with the oracle's, and the outputs of all 32 query heads with the
+    oracle's attention over all 32769 tokens."""
+    w = W.WORKLOADS[1]
+    cal = stored_calib(1)
+    gc = GpuCache(w, cal)
+    n = int(gc.lens[0])
+    r = oracle_encode(w, cal, 0, 0, n + 1)
+    gc.write_codes(0, 0, r.kc[:n], r.vc[:n])
+    q = W.queries(w)
+    got = gc.step(q)                                  # appends token n, attends over n + 1
+    assert gc.device_status() == 0
+    log = []
+    kc, vc = gc.codes(0, n, n + 1)
+    ties = compare_codes(kc, r.kc[n:], r.kx[n:], cal.ck, w.k_sub, "cfg1/step/k", log)
+    ties += compare_codes(vc, r.vc[n:], r.vx[n:], cal.cv, w.v_sub, "cfg1/step/v", log)
+    write_tie_log("full_cfg1_step", log)
+    ref = oracle_attention(w, cal, q[0], r.kc, r.vc)
+    if ties == 0:
+        check_outputs(got[0], ref, "cfg1 decode step, all heads")
+    else:
+        skip_end_to_end("cfg1 decode step", ties)
+        gc.write_codes(0, n, r.kc[n:], r.vc[n:])
+        check_outputs(gc.decode(q), ref[None], "cfg1 attention on oracle codes, all heads")

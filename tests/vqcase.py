@@ -21,6 +21,16 @@ TIE_REL = 1e-6        # ties: centroid distances within 1e-6 relative (see tie_b
 MAX_ABS = 2e-3        # attention output tolerance, fp16 inputs / fp32 accumulation
 MEAN_ABS = 2e-4
 
+# What the parity tests compared, printed at the end of the pytest run
+# (conftest.py): codes compared and in-band ties per check, and end-to-end
+# output rows that were not compared because their codes held a tie.
+PARITY_NOTES: List[str] = []
+CHECKS = {"codes": 0, "code_ties": 0, "outputs": 0, "e2e_skipped": 0}
+
+
+def note(msg: str) -> None:
+    PARITY_NOTES.append(msg)
+
 
 @dataclass
 class Calib:
@@ -106,6 +116,10 @@ def compare_codes(gpu: np.ndarray, orc: np.ndarray, x: np.ndarray, C: np.ndarray
     """Asserts bit-exact codes except in-band ties; returns the number of ties."""
     assert gpu.shape == orc.shape, (gpu.shape, orc.shape)
     mism = np.argwhere(gpu != orc)
+    CHECKS["codes"] += int(gpu.size)
+    CHECKS["code_ties"] += int(len(mism))
+    if len(mism):
+        note(f"codes {label}: {gpu.size} compared, {len(mism)} in-band ties")
     if len(mism) == 0:
         return 0
     xs = x.reshape(x.shape[:-1] + (x.shape[-1] // d, d))
@@ -134,7 +148,17 @@ def write_tie_log(name: str, rows: list) -> Optional[str]:
     return path
 
 
+def skip_end_to_end(label: str, ties: int) -> None:
+    """Records an end-to-end output check left out because the codes held ties
+    (two centroids within the tie band can be far apart, so the outputs may
+    differ by more than the tolerance); the same rows are still checked on the
+    oracle's codes."""
+    CHECKS["e2e_skipped"] += 1
+    note(f"end-to-end rows not compared ({ties} code ties): {label}")
+
+
 def check_outputs(got: np.ndarray, ref: np.ndarray, label: str) -> Tuple[float, float]:
+    CHECKS["outputs"] += int(got.size)
     err = np.abs(got.astype(np.float64) - ref)
     mx, mean = float(err.max()) if err.size else 0.0, float(err.mean()) if err.size else 0.0
     assert mx <= MAX_ABS and mean <= MEAN_ABS, f"{label}: max-abs {mx:.3e}, mean-abs {mean:.3e}"
