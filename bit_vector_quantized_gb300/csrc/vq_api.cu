@@ -363,13 +363,14 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
   p.qscale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 / std::sqrt(128.0));
 
   const int optin = device_smem_optin();
-  // Pipeline stages: the most (up to 8) that fit, and never fewer than the
-  // producer warps.  A producer waits for its slot to be released by the
-  // parity of the slot's "empty" barrier, which tells adjacent phases apart
-  // only; with at least as many stages as producer warps, the producer's own
-  // previous stage guarantees the barrier is at most one phase behind.
+  // Pipeline stages: the most (up to kMaxStages) that fit, and never fewer
+  // than the producer warps.  A producer waits for its slot to be released by
+  // the parity of the slot's "empty" barrier, which tells adjacent phases
+  // apart only; with at least as many stages as producer warps, the
+  // producer's own previous stage guarantees the barrier is at most one phase
+  // behind.
   auto stages_for = [&](const vqk::DecodeShape& sh, size_t& bytes) {
-    int ns = 8;
+    int ns = vqk::kMaxStages;
     for (; ns >= vqk::kProducerWarps; --ns) {
       bytes = vqk::decode_smem(L.k_bits, L.v_bits, p.group, p.k_row, p.v_row, ns, sh.warps,
                                sh.stage_tok()).total;
@@ -377,30 +378,27 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
     }
     return 0;
   };
-  // Consumer shape: 12 warps x 1 chunk for G <= 4, 8 warps x 1 chunk for
-  // G > 4 (register budget), and 8 x 1 wherever 12 x 1 leaves room for fewer
-  // than kProducerWarps stages; VQ_DECODE_SHAPE=8x1|8x2|12x1 selects a shape
-  // explicitly (a tuning switch for profiling; an explicit shape that does not
-  // fit is an error).
-  vqk::DecodeShape shape = p.group > 4 ? vqk::DecodeShape{8, 1} : vqk::DecodeShape{12, 1};
+  // Consumer shape: 12 warps for G <= 4, 8 warps for G > 4 (register
+  // budget), and 8 wherever 12 leaves room for fewer than kProducerWarps
+  // stages; VQ_DECODE_SHAPE=8x1|12x1 selects a shape explicitly (a tuning
+  // switch for profiling; an explicit shape that does not fit is an error).
+  vqk::DecodeShape shape = p.group > 4 ? vqk::DecodeShape{8} : vqk::DecodeShape{12};
   bool explicit_shape = false;
   if (const char* env = std::getenv("VQ_DECODE_SHAPE")) {
-    if (std::strcmp(env, "8x2") == 0) shape = vqk::DecodeShape{8, 2}, explicit_shape = true;
-    if (std::strcmp(env, "8x1") == 0) shape = vqk::DecodeShape{8, 1}, explicit_shape = true;
-    if (std::strcmp(env, "12x1") == 0) shape = vqk::DecodeShape{12, 1}, explicit_shape = true;
+    if (std::strcmp(env, "8x1") == 0) shape = vqk::DecodeShape{8}, explicit_shape = true;
+    if (std::strcmp(env, "12x1") == 0) shape = vqk::DecodeShape{12}, explicit_shape = true;
   }
   int nstage = stages_for(shape, smem);
   if (nstage == 0 && !explicit_shape && shape.warps != 8) {
-    shape = vqk::DecodeShape{8, 1};
+    shape = vqk::DecodeShape{8};
     nstage = stages_for(shape, smem);
   }
   if (nstage == 0)
     return fail(VQ_ERR_UNSUPPORTED,
-                "decode pipeline does not fit: %d consumer warps x %d chunks need %zu bytes of shared "
-                "memory for %d stages",
-                shape.warps, shape.chunks, smem, vqk::kProducerWarps);
+                "decode pipeline does not fit: %d consumer warps need %zu bytes of shared memory "
+                "for %d stages",
+                shape.warps, smem, vqk::kProducerWarps);
   p.warps = shape.warps;
-  p.chunks = shape.chunks;
   p.nstage = nstage;
   return VQ_OK;
 }

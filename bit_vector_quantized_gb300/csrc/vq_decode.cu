@@ -217,46 +217,74 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory");
 }
 
-// Pipeline stages of one work unit.  A unit covers 32-token blocks [a, b) of
-// its sequence (split boundaries from max_seq_len), clipped to the sequence
-// length; stage j holds its tokens [t0, tend) with t0 = 32 a + kStageTok j.
+// First 32-token block of split s: split s covers blocks
+// [s q + min(s, r), (s + 1) q + min(s + 1, r)) of the max_seq_len / 32 blocks
+// (q, r: their quotient and remainder by the split count).
+__device__ __forceinline__ int split_first_block(const DecodeParams& p, int s) {
+  return s * p.split_q + min(s, p.split_r);
+}
+
+// Pipeline stages of one work unit.  A unit covers its split's 32-token
+// blocks, clipped to the sequence length; stage j holds its tokens
+// [t0, tend) with t0 = t_begin + kStageTok j.
 struct UnitStages {
-  int b, kvh, s, len, t_begin, t_end, count;
+  int b, kvh, s, t_begin, t_end, count;
 };
 
 template <int kStageTok>
 __device__ __forceinline__ UnitStages unit_stages(const DecodeParams& p, int k, int len) {
   const UnitId id = unit_id(p, k);
-  // split s covers 32-token blocks [s q + min(s, r), (s + 1) q + min(s + 1, r)) of the
-  // max_seq_len / 32 blocks (q, r: their quotient and remainder by the split count)
-  const int a = id.s * p.split_q + min(id.s, p.split_r);
+  const int a = split_first_block(p, id.s);
   const int b = a + p.split_q + (id.s < p.split_r ? 1 : 0);
   UnitStages u;
   u.b = id.b;
   u.kvh = id.kvh;
   u.s = id.s;
-  u.len = len;
   u.t_begin = a * kUnitTok;
   u.t_end = min(b * kUnitTok, len);
   u.count = u.t_end > u.t_begin ? (u.t_end - u.t_begin + kStageTok - 1) / kStageTok : 0;
   return u;
 }
 
-template <int DK, int BK, int DV, int BV, int NG, int NW, int kNCH>
+// Packed code-row bytes of a format: (128 / d) codes of b bits, rounded up to 4 bytes.
+template <int D, int B>
+struct RowBytes {
+  static constexpr int value = (((kHeadDim / D) * B + 7) / 8 + 3) / 4 * 4;
+};
+
+// log2 of the tokens of one bulk-copy piece: the largest 16 * 2^i that
+// divides the page size with at most 4 KB of rows, so a piece never crosses
+// a page.
+__device__ __forceinline__ int piece_log2(int page_size, int row) {
+  int t = kChunk;
+  while (t * 2 <= page_size && page_size % (t * 2) == 0 && t * 2 * row <= 4096) t *= 2;
+  return __ffs(t) - 1;
+}
+
+// A producer lane's piece of a stage: lanes 0..15 take the K pieces, lanes
+// 16..31 the V pieces, piece i of a tensor being the i-th piece-grid cell the
+// stage touches.  Its first token depends only on the stage's first token, so
+// its page can be looked up before the sequence length is known.
+__device__ __forceinline__ int piece_lo(int t0, int lane, int l2) {
+  return max(t0, ((t0 >> l2) + (lane & 15)) << l2);
+}
+
+template <int DK, int BK, int DV, int BV, int NG, int NW>
 __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split_kernel(const DecodeParams p) {
   static_assert(BK == 8 || (DK == 8 && BK == 12 && DV == 8 && BV == 12),
                 "K codes are byte-aligned, or the 1.5-bit format (d = 8, 12-bit codes)");
   constexpr bool kWide = DK == 8;            // 1.5-bit format: 32-byte table rows, no replicas
   static_assert(NG == 4 || NG == 8, "query heads per pass");
-  static_assert(kNCH == 1 || kNCH == 2, "chunks per consumer warp");
   constexpr int NGL = NG == 4 ? 1 : 2;       // heads owned by one lane
   constexpr int NP = kProducerWarps;
-  constexpr int kSlice = kNCH * kChunk;      // tokens per consumer warp per stage
-  constexpr int kStageTok = NW * kSlice;     // tokens per pipeline stage
+  constexpr int kStageTok = NW * kChunk;     // tokens per pipeline stage (one chunk per consumer warp)
+  constexpr int KROW = RowBytes<DK, BK>::value, VROW = RowBytes<DV, BV>::value;
+  constexpr int kStageBytes = kStageTok * (KROW + VROW);
+  constexpr int kConsumerThreads = NW * 32;
   uint8_t* const smem = g_smem;
   const int G = p.group;
-  const int NS = p.nstage;  // kProducerWarps .. 8 stages
-  const DecodeSmem L = decode_smem(BK, BV, G, p.k_row, p.v_row, NS, NW, kStageTok);
+  const int NS = p.nstage;
+  const DecodeSmem L = decode_smem(BK, BV, G, KROW, VROW, NS, NW, kStageTok);
   float* qt = reinterpret_cast<float*>(smem + L.qt);
   float* merge = reinterpret_cast<float*>(smem + L.merge);
   float2* mlbuf = reinterpret_cast<float2*>(smem + L.ml);
@@ -270,15 +298,72 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_trigger();
-  const int stage_bytes = kStageTok * (p.k_row + p.v_row);
   const int n_units = (p.num_units - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                       static_cast<int>(gridDim.x);
   auto clamp_len = [&](int len) { return len < 0 ? 0 : (len > p.max_seq_len ? p.max_seq_len : len); };
-
-  if (NS < NP || NS > 8) {  // the slot hand-off needs NS >= NP (the host never launches otherwise)
+  // the slot hand-off needs NS >= NP; the rows must be the format's (the host never launches otherwise)
+  if (NS < NP || NS > kMaxStages || p.k_row != KROW || p.v_row != VROW) {
     pdl_wait();
     if (tid == 0) report(p.status, kDevBadConfig);
     return;
+  }
+
+  // ---- every global load of the prologue goes out first -----------------------
+  // The loads of one round trip: codebooks, the first unit's query and lambda,
+  // the units' sequence lengths and the first page of each producer lane's
+  // first piece.  Only inputs of the call are read here (none of them is
+  // written by the previous kernel of the call).
+  constexpr int kNK = kWide ? 1 : ((1 << BK) + kConsumerThreads - 1) / kConsumerThreads;
+  constexpr int kNV = kWide ? 1 : ((1 << BV) + kConsumerThreads - 1) / kConsumerThreads;
+  constexpr int kNB = kNK > kNV ? kNK : kNV;
+  uint2 cbk_r[kNB], cbv_r[kNB];  // centroid tid + i * kConsumerThreads (i < kNK, kNV)
+  uint2 q_r = make_uint2(0, 0);
+  float4 lam_r = make_float4(0.f, 0.f, 0.f, 0.f);
+  int len_r[2] = {0, 0};
+  int page_r = -1, lk = 0, lv = 0;
+  auto load_q = [&](int k) {  // query and lambda of unit k (consumer warps < G)
+    if (warp < G && k < n_units) {
+      const UnitId id = unit_id(p, k);
+      q_r = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.q) +
+                                               (static_cast<long long>(id.b) * p.hq + id.kvh * G + warp) * kHeadDim) +
+                  lane);
+      lam_r = __ldg(reinterpret_cast<const float4*>(p.lambda + id.kvh * kHeadDim) + lane);
+    }
+  };
+  if (warp < NW) {
+#pragma unroll
+    for (int i = 0; i < kNK; ++i) {
+      const int j = tid + i * kConsumerThreads;
+      if (!kWide && j < (1 << BK)) {
+        if constexpr (DK == 4) cbk_r[i] = __ldg(reinterpret_cast<const uint2*>(p.cb_k) + j);
+        else cbk_r[i].x = __ldg(reinterpret_cast<const uint32_t*>(p.cb_k) + j);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kNV; ++i) {
+      const int j = tid + i * kConsumerThreads;
+      if (!kWide && j < (1 << BV)) {
+        if constexpr (DV == 4) cbv_r[i] = __ldg(reinterpret_cast<const uint2*>(p.cb_v) + j);
+        else cbv_r[i].x = __ldg(reinterpret_cast<const uint32_t*>(p.cb_v) + j);
+      }
+    }
+    if (tid < n_units) len_r[0] = __ldg(p.seq_lens + unit_id(p, tid).b);
+    load_q(0);
+  } else {
+    const int ptid = tid - NW * 32, pw = warp - NW;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int k = ptid + i * NP * 32;
+      if (k < n_units) len_r[i] = __ldg(p.seq_lens + unit_id(p, k).b);
+    }
+    lk = piece_log2(p.page_size, KROW);
+    lv = piece_log2(p.page_size, VROW);
+    if (n_units > 0) {  // this lane's piece of stage pw of the first unit, at full length
+      const UnitId id = unit_id(p, 0);
+      const int t0 = split_first_block(p, id.s) * kUnitTok + pw * kStageTok;
+      const int pi = piece_lo(t0, lane, lane < 16 ? lk : lv) / p.page_size;
+      if (pi < p.max_pages) page_r = __ldg(p.page_table + static_cast<long long>(id.b) * p.max_pages + pi);
+    }
   }
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -292,31 +377,24 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
 
   if (warp >= NW) {
     // =========================== producer warps ==============================
-    // Producer warp pw = warp - NW owns stages n = pw, pw + NP, pw + 2 NP, ...;
-    // stage n goes to slot n % NS.  The stage's K rows and V rows are cut into
-    // pieces of at most ~4 KB on a token grid that divides the page size (a
-    // piece never crosses a page); lane i looks up the page of piece i and,
-    // after lane 0 has armed the slot's full barrier with the byte count,
-    // issues that piece as one bulk copy.  A warp issuing bulk copies stalls
-    // while the copy engine accepts them, so several producer warps together
-    // keep enough bytes in flight to reach HBM bandwidth.
-    const int pw = warp - NW;
-    if (pw == 0 && n_units > 0) {  // pull the first unit's page-table entries into L1
-      const UnitId id0 = unit_id(p, 0);
-      const int pg = (id0.s * p.split_q + min(id0.s, p.split_r)) * kUnitTok / p.page_size + lane;
-      if (pg < p.max_pages)
-        asm volatile("prefetch.global.L1 [%0];" ::"l"(p.page_table + static_cast<long long>(id0.b) * p.max_pages + pg));
+    // Producer warp pw = warp - NW owns stages n = pw, pw + NP, pw + 2 NP, ...
+    // (numbered over the CTA's units); stage n goes to slot n % NS.  Lane i
+    // copies piece i & 15 of the K (i < 16) or V (i >= 16) rows as one bulk
+    // copy after lane 0 has armed the slot's full barrier with the byte count.
+    // A warp issuing bulk copies stalls while the copy engine accepts them, so
+    // several producer warps together keep enough bytes in flight to reach
+    // HBM bandwidth.  The page of a lane's next piece is looked up right after
+    // its current issue, so the lookup overlaps the wait for the next slot.
+    const int pw = warp - NW, ptid = tid - NW * 32;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int k = ptid + i * NP * 32;
+      if (k < n_units) ulen_p[k] = clamp_len(len_r[i]);
     }
-    for (int k = tid - NW * 32; k < n_units; k += NP * 32)
-      ulen_p[k] = clamp_len(__ldg(p.seq_lens + unit_id(p, k).b));
     producer_sync<NP>();
     const int P = p.page_size;
-    auto piece_tok = [&](int row) {  // largest 16 * 2^i dividing P with <= 4 KB
-      int t = kChunk;
-      while (t * 2 <= P && P % (t * 2) == 0 && t * 2 * row <= 4096) t *= 2;
-      return t;
-    };
-    const int lk = __ffs(piece_tok(p.k_row)) - 1, lv = __ffs(piece_tok(p.v_row)) - 1;
+    const int l2 = lane < 16 ? lk : lv;
+    const int row = lane < 16 ? KROW : VROW;
     struct It {  // stage iterator over (unit k, stage j), skipping empty units
       int k, j;
       UnitStages u;
@@ -329,46 +407,31 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       }
     };
     auto skip = [&](It& it) {  // advance by NP stages
+#pragma unroll 1
       for (int i = 0; i < NP && it.k < n_units; ++i) {
         ++it.j;
         it_seek(it);
       }
     };
-    struct Piece {  // this lane's piece of a stage: tensor (0 = K, 1 = V), tokens
-      int which, t_lo, t_hi;
-    };
-    auto piece_of = [&](const UnitStages& su, int sj) -> Piece {
-      const int t0 = su.t_begin + sj * kStageTok;
-      const int tend16 = (min(t0 + kStageTok, su.t_end) + kChunk - 1) & ~(kChunk - 1);
-      const int nk = ((tend16 - 1) >> lk) - (t0 >> lk) + 1;
-      Piece pc;
-      pc.which = lane < nk ? 0 : 1;
-      const int l2 = pc.which == 0 ? lk : lv;
-      const int idx = (t0 >> l2) + (pc.which == 0 ? lane : lane - nk);
-      pc.t_lo = max(t0, idx << l2);
-      pc.t_hi = min(tend16, (idx + 1) << l2);
-      return pc;
-    };
     auto lookup = [&](const It& it) -> int {  // page of this lane's piece of stage `it`
       if (it.k >= n_units) return -1;
-      const Piece pc = piece_of(it.u, it.j);
-      if (pc.t_lo >= pc.t_hi) return -1;
-      const int pi = pc.t_lo / P;
+      const int pi = piece_lo(it.u.t_begin + it.j * kStageTok, lane, l2) / P;
       return pi < p.max_pages ? __ldg(p.page_table + static_cast<long long>(it.u.b) * p.max_pages + pi) : -1;
     };
     auto issue = [&](const UnitStages& su, int sj, int page, int n) {
       const int slot = n % NS;
       const int t0 = su.t_begin + sj * kStageTok;
       const int tend = min(t0 + kStageTok, su.t_end);
-      const Piece pc = piece_of(su, sj);
-      const bool has = pc.t_lo < pc.t_hi;
+      const int tend16 = (tend + kChunk - 1) & ~(kChunk - 1);
+      const int t_lo = piece_lo(t0, lane, l2);
+      const int t_hi = min(tend16, ((t0 >> l2) + (lane & 15) + 1) << l2);
+      const bool has = t_lo < t_hi;
       const bool ok = has && page >= 0 && page < p.num_pages;
       if (has && !ok) report(p.status, kDevBadPage);
-      const int row = pc.which == 0 ? p.k_row : p.v_row;
-      const uint32_t bytes = ok ? static_cast<uint32_t>(pc.t_hi - pc.t_lo) * row : 0u;
+      const uint32_t bytes = ok ? static_cast<uint32_t>(t_hi - t_lo) * row : 0u;
       uint32_t mask = 0;  // 16-token chunks with data (from the K pieces)
-      if (ok && pc.which == 0) {
-        const int c0 = (pc.t_lo - t0) / kChunk, c1 = (pc.t_hi - t0) / kChunk;
+      if (ok && lane < 16) {
+        const int c0 = (t_lo - t0) / kChunk, c1 = (t_hi - t0) / kChunk;
         mask = ((1u << c1) - 1u) & ~((1u << c0) - 1u);
       }
       const uint32_t total = __reduce_add_sync(kFull, bytes);
@@ -380,44 +443,36 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       }
       __syncwarp();
       if (ok) {
-        uint8_t* dst = stages + static_cast<size_t>(slot) * stage_bytes +
-                       (pc.which == 0 ? 0 : kStageTok * p.k_row) + (pc.t_lo - t0) * row;
-        const uint8_t* pool = pc.which == 0 ? p.k_pool : p.v_pool;
-        const long long row0 = (static_cast<long long>(page) * p.hkv + su.kvh) * P + (pc.t_lo % P);
-        bulk_copy_g2s(dst, pool + row0 * row, (pc.t_hi - pc.t_lo) * row, full + slot);
+        uint8_t* dst = stages + static_cast<size_t>(slot) * kStageBytes +
+                       (lane < 16 ? 0 : kStageTok * KROW) + (t_lo - t0) * row;
+        const uint8_t* pool = lane < 16 ? p.k_pool : p.v_pool;
+        const long long row0 = (static_cast<long long>(page) * p.hkv + su.kvh) * P + (t_lo % P);
+        bulk_copy_g2s(dst, pool + row0 * row, (t_hi - t_lo) * row, full + slot);
       }
     };
-    // Page numbers run 4 of this warp's stages ahead of its copies: ring[i]
-    // holds the pages of its next stage with index % 4 == i.
     It cur;
     cur.k = 0;
     cur.j = 0;
     if (n_units > 0) cur.u = unit_stages<kStageTok>(p, 0, ulen_p[0]);
     it_seek(cur);
+#pragma unroll 1
     for (int i = 0; i < pw && cur.k < n_units; ++i) {
       ++cur.j;
       it_seek(cur);
     }
-    It ahead = cur;
-    int ring[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      ring[i] = lookup(ahead);
-      skip(ahead);
-    }
+    // the page looked up at entry is this stage's unless the first unit was too short
+    int page = (cur.k == 0 && cur.j == pw) ? page_r : lookup(cur);
     pdl_wait();  // the pools may be written by the previous kernel: copy only after it
     int n = pw;
     bool stop = false;
-    while (cur.k < n_units && !stop) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (cur.k >= n_units || stop) break;
-        const int slot = n % NS;
-        if (n >= NS) {  // wait until the consumers have released the slot
-          const uint32_t par = static_cast<uint32_t>(n / NS - 1) & 1u;
-          bool ok = !*abort_flag && mbar_wait_bounded(empty + slot, par, abort_flag, p.timeout_ns);
-          ok = __all_sync(kFull, ok);
-          if (!ok) {
+    while (cur.k < n_units) {
+      const int slot = n % NS;
+      if (n >= NS) {  // wait until the consumers have released the slot
+        const uint32_t par = static_cast<uint32_t>(n / NS - 1) & 1u;
+        bool ok = mbar_try_wait(empty + slot, par);
+        if (!__all_sync(kFull, ok)) {
+          ok = !*abort_flag && mbar_wait_bounded(empty + slot, par, abort_flag, p.timeout_ns);
+          if (!__all_sync(kFull, ok)) {
             if (lane == 0 && !*abort_flag) {
               *abort_flag = 1;
               report(p.status, kDevTimeout);
@@ -426,15 +481,14 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
             break;
           }
         }
-        issue(cur.u, cur.j, ring[i], n);
-        ring[i] = lookup(ahead);
-        skip(ahead);
-        n += NP;
-        skip(cur);
       }
+      issue(cur.u, cur.j, page, n);
+      skip(cur);
+      page = lookup(cur);
+      n += NP;
     }
     __syncthreads();  // every consumer is done
-    if (*abort_flag && lane == 0) {  // wait (bounded) for this warp's copies still in flight
+    if (stop && lane == 0) {  // wait (bounded) for this warp's copies still in flight
       for (int i = n - NP; i >= 0 && i >= n - NS - NP; i -= NP) {
         volatile int no_abort = 0;
         mbar_wait_bounded(full + i % NS, static_cast<uint32_t>(i / NS) & 1u, &no_abort,
@@ -445,43 +499,10 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   }
 
   // ============================= consumer warps ==============================
-  constexpr int kConsumerThreads = NW * 32;
-  // replicated tables: each thread's centroids are loaded here, stored after
-  // the query loads have gone out (the wide table is copied in one pass below)
-  constexpr int kNK = kWide ? 1 : ((1 << BK) + kConsumerThreads - 1) / kConsumerThreads;
-  constexpr int kNV = kWide ? 1 : ((1 << BV) + kConsumerThreads - 1) / kConsumerThreads;
-  uint2 cbk_r[kNK], cbv_r[kNV];
-#pragma unroll
-  for (int i = 0; i < kNK; ++i) {
-    const int j = tid + i * kConsumerThreads;
-    if (!kWide && j < (1 << BK)) {
-      if constexpr (DK == 4) cbk_r[i] = __ldg(reinterpret_cast<const uint2*>(p.cb_k) + j);
-      else cbk_r[i].x = __ldg(reinterpret_cast<const uint32_t*>(p.cb_k) + j);
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < kNV; ++i) {
-    const int j = tid + i * kConsumerThreads;
-    if (!kWide && j < (1 << BV)) {
-      if constexpr (DV == 4) cbv_r[i] = __ldg(reinterpret_cast<const uint2*>(p.cb_v) + j);
-      else cbv_r[i].x = __ldg(reinterpret_cast<const uint32_t*>(p.cb_v) + j);
-    }
-  }
-  int len_r = 0;
-  if (tid < n_units) len_r = __ldg(p.seq_lens + unit_id(p, tid).b);
-  uint2 q_r = make_uint2(0, 0);
-  float4 lam_r = make_float4(0.f, 0.f, 0.f, 0.f);
-  auto load_q = [&](int k) {  // query and lambda of unit k (consumer warps < G)
-    if (warp < G && k < n_units) {
-      const UnitId id = unit_id(p, k);
-      q_r = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.q) +
-                                               (static_cast<long long>(id.b) * p.hq + id.kvh * G + warp) * kHeadDim) +
-                  lane);
-      lam_r = __ldg(reinterpret_cast<const float4*>(p.lambda + id.kvh * kHeadDim) + lane);
-    }
-  };
-  load_q(0);
-  if constexpr (kWide) {  // half-major table: [tensor][half][code] x 8 bytes (see row12)
+  // Codebook table: row j = 16 copies of 8-byte (32 copies of 4-byte) K
+  // centroid j, then the same for V centroid j; the 1.5-bit format's table is
+  // half-major ([tensor][half][code] x 8 bytes, see row12), copied in one pass.
+  if constexpr (kWide) {
     const uint32_t tab = smem_addr(smem + L.tab);
     constexpr int kBatch = 4;  // loads in flight per thread
     for (int j0 = tid; j0 < (1 << BK); j0 += kBatch * kConsumerThreads) {
@@ -508,44 +529,67 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
         }
       }
     }
-  } else {  // codebook table: row j = 16 copies of 8-byte (32 copies of 4-byte) K centroid j,
-            // then the same for V centroid j
+  } else {
+    // Warp w holds centroids 32 b + lane of blocks b = w, w + NW, ... (loaded
+    // at entry).  One store instruction fills 128 contiguous bytes of one or
+    // two rows, so no two lanes share a bank: the replicas of centroid row i
+    // reach the lanes by shuffle.
     const uint32_t tab = smem_addr(smem + L.tab);
+    auto fill = [&](const uint2 (&cb)[kNB], int n_i, int rows, int d, uint32_t half) {
 #pragma unroll
-    for (int i = 0; i < kNK; ++i) {
-      const int j = tid + i * kConsumerThreads;
-      if (j < (1 << BK)) {
-        if constexpr (DK == 4) {
-#pragma unroll
-          for (int rep = 0; rep < 16; ++rep)
-            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(tab + j * kTabRow + rep * 8),
-                         "r"(cbk_r[i].x), "r"(cbk_r[i].y));
-        } else {
-#pragma unroll
-          for (int rep = 0; rep < 32; ++rep)
-            asm volatile("st.shared.u32 [%0], %1;" ::"r"(tab + j * kTabRow + rep * 4), "r"(cbk_r[i].x));
+      for (int i = 0; i < kNB; ++i) {
+        const int block = warp + i * NW;
+        if (i >= n_i || block * 32 >= rows) break;
+        if (d == 4) {  // two rows per store: lanes 0..15 row 2 t, lanes 16..31 row 2 t + 1
+#pragma unroll 4
+          for (int t = 0; t < 16; ++t) {
+            const int src = 2 * t + (lane >> 4);
+            const uint32_t x = __shfl_sync(kFull, cb[i].x, src), y = __shfl_sync(kFull, cb[i].y, src);
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(tab + (block * 32 + src) * kTabRow + half +
+                                                                  (lane & 15) * 8),
+                         "r"(x), "r"(y));
+          }
+        } else {       // one row per store: lane l writes replica l
+#pragma unroll 4
+          for (int t = 0; t < 32; ++t) {
+            const uint32_t x = __shfl_sync(kFull, cb[i].x, t);
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(tab + (block * 32 + t) * kTabRow + half + lane * 4),
+                         "r"(x));
+          }
         }
       }
-    }
-#pragma unroll
-    for (int i = 0; i < kNV; ++i) {
-      const int j = tid + i * kConsumerThreads;
-      if (j < (1 << BV)) {
-        if constexpr (DV == 4) {
-#pragma unroll
-          for (int rep = 0; rep < 16; ++rep)
-            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(tab + j * kTabRow + 128 + rep * 8),
-                         "r"(cbv_r[i].x), "r"(cbv_r[i].y));
-        } else {
-#pragma unroll
-          for (int rep = 0; rep < 32; ++rep)
-            asm volatile("st.shared.u32 [%0], %1;" ::"r"(tab + j * kTabRow + 128 + rep * 4), "r"(cbv_r[i].x));
-        }
-      }
-    }
+    };
+    fill(cbk_r, kNK, 1 << BK, DK, 0u);
+    fill(cbv_r, kNV, 1 << BV, DV, 128u);
   }
-  if (tid < n_units) ulen_c[tid] = clamp_len(len_r);
-  consumer_sync<NW>();  // codebooks and unit lengths visible to the consumers
+  if (tid < n_units) ulen_c[tid] = clamp_len(len_r[0]);
+
+  // q~ = q diag(lambda) H_D * scale * log2(e), split into fp16 hi + lo parts
+  // and stored in the score mma's B-operand order: table [head][hi, lo][c][16
+  // words], words 2kk, 2kk+1 = dims 32c + 4kk + {0, 1} and {2, 3} (lane l of
+  // the head's warp holds dims 4l .. 4l+3, i.e. c = l / 8, kk = l % 8).  Heads
+  // G .. NG-1 are zeros.  The consumers then read their operands with a few
+  // 16-byte loads.
+  auto transform_query = [&](int k) {
+    if (warp < NG) {
+      uint32_t h01 = 0u, l01 = 0u, h23 = 0u, l23 = 0u;
+      if (warp < G) {
+        const __half2 lo = *reinterpret_cast<const __half2*>(&q_r.x);
+        const __half2 hi = *reinterpret_cast<const __half2*>(&q_r.y);
+        float x[4] = {__low2float(lo) * lam_r.x, __high2float(lo) * lam_r.y,
+                      __low2float(hi) * lam_r.z, __high2float(hi) * lam_r.w};
+        fwht128_warp(x, lane);
+        split_half2(x[0] * p.qscale, x[1] * p.qscale, h01, l01);
+        split_half2(x[2] * p.qscale, x[3] * p.qscale, h23, l23);
+        load_q(k + 1);  // prefetch the next unit's query
+      }
+      uint32_t* qf = reinterpret_cast<uint32_t*>(qt) + (warp * 2 * 4 + (lane >> 3)) * 16 + 2 * (lane & 7);
+      *reinterpret_cast<uint2*>(qf) = make_uint2(h01, h23);
+      *reinterpret_cast<uint2*>(qf + 4 * 16) = make_uint2(l01, l23);
+    }
+  };
+  transform_query(0);
+  consumer_sync<NW>();  // codebook table, unit lengths and the first unit's q~ visible
 
   const int r = lane >> 2, c = lane & 3;
   // the lane's byte inside a table row: its replica of the K (bytes 0..127)
@@ -558,38 +602,41 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   float m_run[NGL], l_run[NGL];
 
   // ---- code registers -------------------------------------------------------
-  // K: tokens r and r+8 of a chunk.  V (G <= 4): tokens c, c+4, c+8, c+12;
-  // V (G > 4): tokens 2c, 2c+1, 2c+8, 2c+9, and with 32-byte rows lanes c >= 2
-  // read each pair swapped so that every load hits 32 different banks (the
-  // PRMT selectors undo the swap).
+  // K: tokens r and r+8 of the warp's chunk.  V (G <= 4): tokens c, c+4, c+8,
+  // c+12; V (G > 4): tokens 2c, 2c+1, 2c+8, 2c+9, and with 32-byte rows lanes
+  // c >= 2 read each pair swapped so that every load hits 32 different banks
+  // (the PRMT selectors undo the swap).
   constexpr bool kSwap = NG == 8 && DV == 4 && BV == 8;
   const int sw = (kSwap && c >= 2) ? 1 : 0;
   const uint32_t sel_lo = sw ? 0x1054u : 0x5410u, sel_hi = sw ? 0x3276u : 0x7632u;
-  KCodes<DK> kc[kNCH][2];          // current stage
-  VCodes<DV, BV> vc[kNCH][4];      // current stage
-  VCodes<DV, BV> pvc[kNCH][4];     // previous stage, P.V pending
-  uint32_t pb[kNCH][2][2];         // previous stage's P operands [chunk][k-step or token pair][reg]
+  // P operand placement (G <= 4): lane (r, c) puts p into half r & 1 of its
+  // B registers; selectors taking the low / high half of a packed pair
+  const uint32_t sel_p_lo = (r & 1) ? 0x1044u : 0x4410u, sel_p_hi = (r & 1) ? 0x3244u : 0x4432u;
+  KCodes<DK> kc[2];          // current stage
+  VCodes<DV, BV> vc[4];      // current stage
+  VCodes<DV, BV> pvc[4];     // previous stage, P.V pending
+  uint32_t pb[2][2] = {{0u, 0u}, {0u, 0u}};  // previous stage's P operands [k-step or token pair][reg]
 
-  auto load_codes = [&](const uint8_t* st, int off) {
+  // lane-constant byte offsets of the lane's code rows inside a stage
+  const int koff0 = (warp * kChunk + r) * KROW, koff1 = koff0 + 8 * KROW;
+  const int voff = kStageTok * KROW + warp * kChunk * VROW;
+  auto load_codes = [&](const uint8_t* st) {
+    kc[0].load(st + koff0, c);
+    kc[1].load(st + koff1, c);
+    const uint8_t* sv = st + voff;
+    if constexpr (NG == 4) {
 #pragma unroll
-    for (int n = 0; n < kNCH; ++n) {
-      kc[n][0].load(st + (off + n * kChunk + r) * p.k_row, c);
-      kc[n][1].load(st + (off + n * kChunk + r + 8) * p.k_row, c);
-      const uint8_t* sv = st + kStageTok * p.k_row + (off + n * kChunk) * p.v_row;
-      if constexpr (NG == 4) {
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) vc[n][jj].load(sv + (c + 4 * jj) * p.v_row, r);
-      } else {
-        const uint8_t* vr0 = sv + (2 * c) * p.v_row;
-        vc[n][0].load(vr0 + sw * p.v_row, r);
-        vc[n][1].load(vr0 + (1 - sw) * p.v_row, r);
-        vc[n][2].load(vr0 + (8 + sw) * p.v_row, r);
-        vc[n][3].load(vr0 + (9 - sw) * p.v_row, r);
-      }
+      for (int jj = 0; jj < 4; ++jj) vc[jj].load(sv + (c + 4 * jj) * VROW, r);
+    } else {
+      const uint8_t* vr0 = sv + (2 * c) * VROW;
+      vc[0].load(vr0 + sw * VROW, r);
+      vc[1].load(vr0 + (1 - sw) * VROW, r);
+      vc[2].load(vr0 + (8 + sw) * VROW, r);
+      vc[3].load(vr0 + (9 - sw) * VROW, r);
     }
   };
 
-  // P.V of the previous stage's chunks, output step q (0..3 for G <= 4).
+  // P.V of the previous stage's chunk, output step q (0..3 for G <= 4).
   //  G <= 4: the mma reduction index runs over (token t', element e) with
   //    k = 2 t' + e, so one gathered fp16 pair of a centroid is one operand
   //    register; the output column (2g + e') selects element e' of head g.
@@ -598,108 +645,95 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   //    16r + 4q .. 16r + 4q + 3 of head c.
   //  G > 4: reduction over 16 tokens, A = V^T built with PRMT (pairs of tokens).
   auto pv_step = [&](int q) {
+    if constexpr (NG == 4) {
 #pragma unroll
-    for (int n = 0; n < kNCH; ++n) {
-      if constexpr (NG == 4) {
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {  // tokens 8ks + c and 8ks + c + 4
-          uint32_t a0, a1, a2, a3;
-          if constexpr (DV >= 4) {
-            const uint2 w0 = tab64(pvc[n][2 * ks].off(q, lwv));
-            const uint2 w1 = tab64(pvc[n][2 * ks + 1].off(q, lwv));
-            a0 = w0.x; a1 = w0.y; a2 = w1.x; a3 = w1.y;
-          } else {
-            a0 = tab32(pvc[n][2 * ks].off(2 * q, lwv));
-            a1 = tab32(pvc[n][2 * ks].off(2 * q + 1, lwv));
-            a2 = tab32(pvc[n][2 * ks + 1].off(2 * q, lwv));
-            a3 = tab32(pvc[n][2 * ks + 1].off(2 * q + 1, lwv));
-          }
-          mma16816(O[q], a0, a1, a2, a3, pb[n][ks][0], pb[n][ks][1]);
-        }
-      } else {
-        if constexpr (DV >= 4) {  // q = output step pair (2q, 2q+1)
-          uint2 W[4];
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) W[jj] = tab64(pvc[n][jj].off(q, lwv));
-          mma16816(O[2 * q], __byte_perm(W[0].x, W[1].x, sel_lo), __byte_perm(W[0].x, W[1].x, sel_hi),
-                   __byte_perm(W[2].x, W[3].x, sel_lo), __byte_perm(W[2].x, W[3].x, sel_hi), pb[n][0][0],
-                   pb[n][0][1]);
-          mma16816(O[2 * q + 1], __byte_perm(W[0].y, W[1].y, sel_lo), __byte_perm(W[0].y, W[1].y, sel_hi),
-                   __byte_perm(W[2].y, W[3].y, sel_lo), __byte_perm(W[2].y, W[3].y, sel_hi), pb[n][0][0],
-                   pb[n][0][1]);
+      for (int ks = 0; ks < 2; ++ks) {  // tokens 8ks + c and 8ks + c + 4
+        uint32_t a0, a1, a2, a3;
+        if constexpr (DV >= 4) {
+          const uint2 w0 = tab64(pvc[2 * ks].off(q, lwv));
+          const uint2 w1 = tab64(pvc[2 * ks + 1].off(q, lwv));
+          a0 = w0.x; a1 = w0.y; a2 = w1.x; a3 = w1.y;
         } else {
+          a0 = tab32(pvc[2 * ks].off(2 * q, lwv));
+          a1 = tab32(pvc[2 * ks].off(2 * q + 1, lwv));
+          a2 = tab32(pvc[2 * ks + 1].off(2 * q, lwv));
+          a3 = tab32(pvc[2 * ks + 1].off(2 * q + 1, lwv));
+        }
+        mma16816(O[q], a0, a1, a2, a3, pb[ks][0], pb[ks][1]);
+      }
+    } else {
+      if constexpr (DV >= 4) {  // q = output step pair (2q, 2q+1)
+        uint2 W[4];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t W[4];
+        for (int jj = 0; jj < 4; ++jj) W[jj] = tab64(pvc[jj].off(q, lwv));
+        mma16816(O[2 * q], __byte_perm(W[0].x, W[1].x, sel_lo), __byte_perm(W[0].x, W[1].x, sel_hi),
+                 __byte_perm(W[2].x, W[3].x, sel_lo), __byte_perm(W[2].x, W[3].x, sel_hi), pb[0][0],
+                 pb[0][1]);
+        mma16816(O[2 * q + 1], __byte_perm(W[0].y, W[1].y, sel_lo), __byte_perm(W[0].y, W[1].y, sel_hi),
+                 __byte_perm(W[2].y, W[3].y, sel_lo), __byte_perm(W[2].y, W[3].y, sel_hi), pb[0][0],
+                 pb[0][1]);
+      } else {
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) W[jj] = tab32(pvc[n][jj].off(2 * q + h, lwv));
-            mma16816(O[2 * q + h], __byte_perm(W[0], W[1], 0x5410), __byte_perm(W[0], W[1], 0x7632),
-                     __byte_perm(W[2], W[3], 0x5410), __byte_perm(W[2], W[3], 0x7632), pb[n][0][0],
-                     pb[n][0][1]);
-          }
+        for (int h = 0; h < 2; ++h) {
+          uint32_t W[4];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) W[jj] = tab32(pvc[jj].off(2 * q + h, lwv));
+          mma16816(O[2 * q + h], __byte_perm(W[0], W[1], 0x5410), __byte_perm(W[0], W[1], 0x7632),
+                   __byte_perm(W[2], W[3], 0x5410), __byte_perm(W[2], W[3], 0x7632), pb[0][0],
+                   pb[0][1]);
         }
       }
     }
   };
 
-  // One basic block: scores of the current chunks and P.V of the previous
-  // chunks, two independent streams the scheduler interleaves.
-  auto fused = [&](float (&sc)[kNCH][4], bool with_qk) {
-    float acc[kNCH][2][4], acc2[kNCH][2][4];  // [chunk][k-step parity][..]
-#pragma unroll
-    for (int n = 0; n < kNCH; ++n)
-#pragma unroll
-      for (int e = 0; e < 2; ++e)
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) acc[n][e][jj] = acc2[n][e][jj] = 0.f;
+  // One basic block: scores of the current chunk and P.V of the previous
+  // chunk, two independent streams the scheduler interleaves.
+  auto fused = [&](float (&sc)[4], bool with_qk) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       if (with_qk) {
-#pragma unroll
-        for (int n = 0; n < kNCH; ++n) {
-          uint32_t a0, a1, a2, a3;
-          if constexpr (DK >= 4) {
-            const uint2 g0 = tab64(kc[n][0].off(kk, lwk));
-            const uint2 g1 = tab64(kc[n][1].off(kk, lwk));
-            a0 = g0.x; a1 = g1.x; a2 = g0.y; a3 = g1.y;
-          } else {
-            a0 = tab32(kc[n][0].off(2 * kk, lwk));
-            a1 = tab32(kc[n][1].off(2 * kk, lwk));
-            a2 = tab32(kc[n][0].off(2 * kk + 1, lwk));
-            a3 = tab32(kc[n][1].off(2 * kk + 1, lwk));
-          }
-          mma16816(acc[n][kk & 1], a0, a1, a2, a3, qa[kk][0], qa[kk][1]);
-          if constexpr (NG == 8) mma16816(acc2[n][kk & 1], a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        uint32_t a0, a1, a2, a3;
+        if constexpr (DK >= 4) {
+          const uint2 g0 = tab64(kc[0].off(kk, lwk));
+          const uint2 g1 = tab64(kc[1].off(kk, lwk));
+          a0 = g0.x; a1 = g1.x; a2 = g0.y; a3 = g1.y;
+        } else {
+          a0 = tab32(kc[0].off(2 * kk, lwk));
+          a1 = tab32(kc[1].off(2 * kk, lwk));
+          a2 = tab32(kc[0].off(2 * kk + 1, lwk));
+          a3 = tab32(kc[1].off(2 * kk + 1, lwk));
         }
+        mma16816(acc, a0, a1, a2, a3, qa[kk][0], qa[kk][1]);
+        if constexpr (NG == 8) mma16816(acc2, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
       }
       if ((kk & 1) == 0) pv_step(kk >> 1);
     }
 #pragma unroll
-    for (int n = 0; n < kNCH; ++n)
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        sc[n][jj] = acc[n][0][jj] + acc[n][1][jj];
-        if constexpr (NG == 8) sc[n][jj] += acc2[n][0][jj] + acc2[n][1][jj];
-      }
+    for (int jj = 0; jj < 4; ++jj) sc[jj] = NG == 8 ? acc[jj] + acc2[jj] : acc[jj];
   };
 
-  // Online softmax (log2 domain) over the current chunks: updates m and l,
-  // rescales O, and leaves the chunks' P operands (fp16) in pb.  Tokens at or
-  // past `lim`, and chunks whose bit in `live` is clear, get p = 0.
-  auto softmax = [&](const float (&sc)[kNCH][4], int tok0, int lim, uint32_t live) {
-    float s[kNCH][NGL][2];
+  // Online softmax (log2 domain) over the current chunk: updates m and l,
+  // rescales O, and leaves the chunk's P operands (fp16) in pb.  Tokens at or
+  // past `lim` get p = 0, and all of them when `live` is false.
+  auto softmax = [&](const float (&sc)[4], int tok0, int lim, bool live) {
+    float s[NGL][2];
+    if constexpr (NG == 4) {  // columns 2c (hi) + 2c+1 (lo) of head c
+      s[0][0] = sc[0] + sc[1];
+      s[0][1] = sc[2] + sc[3];
+    } else {                  // columns 2c, 2c+1 = heads 2c, 2c+1
+      s[0][0] = sc[0];
+      s[1][0] = sc[1];
+      s[0][1] = sc[2];
+      s[1][1] = sc[3];
+    }
+    if (!live || tok0 + kChunk > lim) {  // warp-uniform: a chunk at the end of the unit, or no data
+      const int lim_n = live ? lim : 0;
+      const bool v0 = tok0 + r < lim_n, v1 = tok0 + r + 8 < lim_n;
 #pragma unroll
-    for (int n = 0; n < kNCH; ++n) {
-      const int t0 = tok0 + n * kChunk + r, t1 = t0 + 8;
-      const int lim_n = ((live >> n) & 1u) ? lim : 0;
-      if constexpr (NG == 4) {  // columns 2c (hi) + 2c+1 (lo) of head c
-        s[n][0][0] = t0 < lim_n ? sc[n][0] + sc[n][1] : -INFINITY;
-        s[n][0][1] = t1 < lim_n ? sc[n][2] + sc[n][3] : -INFINITY;
-      } else {                  // columns 2c, 2c+1 = heads 2c, 2c+1
-        s[n][0][0] = t0 < lim_n ? sc[n][0] : -INFINITY;
-        s[n][1][0] = t0 < lim_n ? sc[n][1] : -INFINITY;
-        s[n][0][1] = t1 < lim_n ? sc[n][2] : -INFINITY;
-        s[n][1][1] = t1 < lim_n ? sc[n][3] : -INFINITY;
+      for (int gi = 0; gi < NGL; ++gi) {
+        s[gi][0] = v0 ? s[gi][0] : -INFINITY;
+        s[gi][1] = v1 ? s[gi][1] : -INFINITY;
       }
     }
     // Lazy running max: m_run moves only when a score exceeds it by more than
@@ -710,11 +744,8 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
     bool grow = false;
 #pragma unroll
     for (int gi = 0; gi < NGL; ++gi) {
-      float mx = -INFINITY;
-#pragma unroll
-      for (int n = 0; n < kNCH; ++n) mx = fmaxf(mx, fmaxf(s[n][gi][0], s[n][gi][1]));
-      lmax[gi] = mx;
-      grow = grow || mx > m_run[gi] + kLazyLog2;
+      lmax[gi] = fmaxf(s[gi][0], s[gi][1]);
+      grow = grow || lmax[gi] > m_run[gi] + kLazyLog2;
     }
     if (__any_sync(kFull, grow)) {
       float alpha[NGL];
@@ -745,36 +776,28 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
 #pragma unroll
     for (int gi = 0; gi < NGL; ++gi) {
       const float mref = m_run[gi] == -INFINITY ? 0.f : m_run[gi];
-      float lsum = 0.f;
-#pragma unroll
-      for (int n = 0; n < kNCH; ++n)
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          s[n][gi][t] = fast_exp2(s[n][gi][t] - mref);
-          lsum += s[n][gi][t];
-        }
-      l_run[gi] += lsum;
+      s[gi][0] = fast_exp2(s[gi][0] - mref);
+      s[gi][1] = fast_exp2(s[gi][1] - mref);
+      l_run[gi] += s[gi][0] + s[gi][1];
     }
+    if constexpr (NG == 4) {
+      // B[k = 2t' + e][col = 2g + e'] = p[t'][g] * (e == e'): lane (r, c) needs
+      // p of head r/2 for tokens c, c+4 (k-step 0) and c+8, c+12 (k-step 1).
+      // Lane (r', c') holds p of head c' for tokens r' and r'+8: packed into one
+      // fp16 pair, two shuffles fetch the pairs of tokens (c, c+8) and (c+4,
+      // c+12), and each operand register takes one half, placed in half r & 1.
+      const uint32_t mine = pack_half2(__float2half_rn(s[0][0]), __float2half_rn(s[0][1]));
+      const uint32_t x = __shfl_sync(kFull, mine, 4 * c + (r >> 1));
+      const uint32_t y = __shfl_sync(kFull, mine, 4 * (c + 4) + (r >> 1));
+      pb[0][0] = __byte_perm(x, 0u, sel_p_lo);
+      pb[0][1] = __byte_perm(y, 0u, sel_p_lo);
+      pb[1][0] = __byte_perm(x, 0u, sel_p_hi);
+      pb[1][1] = __byte_perm(y, 0u, sel_p_hi);
+    } else {
+      // P^T operand: transpose the fp16 pairs (head 2c, 2c+1) of each 8-token block
 #pragma unroll
-    for (int n = 0; n < kNCH; ++n) {
-      if constexpr (NG == 4) {
-        // B[k = 2t' + e][col = 2g + e'] = p[t'][g] * (e == e'): lane (r, c) needs
-        // p of head r/2 for tokens c, c+4 (k-step 0) and c+8, c+12 (k-step 1),
-        // held by lanes 4c + r/2 and 4(c+4) + r/2 (rows r and r+8 of the chunk).
-        const int src0 = 4 * c + (r >> 1), src1 = 4 * (c + 4) + (r >> 1);
-        const float p00 = __shfl_sync(kFull, s[n][0][0], src0), p01 = __shfl_sync(kFull, s[n][0][0], src1);
-        const float p10 = __shfl_sync(kFull, s[n][0][1], src0), p11 = __shfl_sync(kFull, s[n][0][1], src1);
-        const int sh = (r & 1) * 16;
-        pb[n][0][0] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(p00))) << sh;
-        pb[n][0][1] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(p01))) << sh;
-        pb[n][1][0] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(p10))) << sh;
-        pb[n][1][1] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(p11))) << sh;
-      } else {
-        // P^T operand: transpose the fp16 pairs (head 2c, 2c+1) of each 8-token block
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-          pb[n][0][t] = movmatrix_trans(pack_half2(__float2half_rn(s[n][0][t]), __float2half_rn(s[n][NGL - 1][t])));
-      }
+      for (int t = 0; t < 2; ++t)
+        pb[0][t] = movmatrix_trans(pack_half2(__float2half_rn(s[0][t]), __float2half_rn(s[NGL - 1][t])));
     }
   };
 
@@ -782,32 +805,11 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   uint32_t phase = 0u;   // parity of the slot's current fill
   for (int k = 0; k < n_units; ++k) {
     const UnitStages u = unit_stages<kStageTok>(p, k, ulen_c[k]);
-    consumer_sync<NW>();  // previous unit's merge buffers and q~ are free
-    // q~ = q diag(lambda) H_D * scale * log2(e), split into fp16 hi + lo parts
-    // and stored in the score mma's B-operand order: table [head][hi, lo][c][16
-    // words], words 2kk, 2kk+1 = dims 32c + 4kk + {0, 1} and {2, 3} (lane l of
-    // the head's warp holds dims 4l .. 4l+3, i.e. c = l / 8, kk = l % 8).  Heads
-    // G .. NG-1 are zeros.  The consumers then read their operands with a few
-    // 16-byte loads: this per-unit code stays short, which matters because it
-    // runs once per unit, out of an instruction cache the stage loop has just
-    // filled.
-    if (warp < NG) {
-      uint32_t h01 = 0u, l01 = 0u, h23 = 0u, l23 = 0u;
-      if (warp < G) {
-        const __half2 lo = *reinterpret_cast<const __half2*>(&q_r.x);
-        const __half2 hi = *reinterpret_cast<const __half2*>(&q_r.y);
-        float x[4] = {__low2float(lo) * lam_r.x, __high2float(lo) * lam_r.y,
-                      __low2float(hi) * lam_r.z, __high2float(hi) * lam_r.w};
-        fwht128_warp(x, lane);
-        split_half2(x[0] * p.qscale, x[1] * p.qscale, h01, l01);
-        split_half2(x[2] * p.qscale, x[3] * p.qscale, h23, l23);
-        load_q(k + 1);  // prefetch the next unit's query
-      }
-      uint32_t* qf = reinterpret_cast<uint32_t*>(qt) + (warp * 2 * 4 + (lane >> 3)) * 16 + 2 * (lane & 7);
-      *reinterpret_cast<uint2*>(qf) = make_uint2(h01, h23);
-      *reinterpret_cast<uint2*>(qf + 4 * 16) = make_uint2(l01, l23);
+    if (k > 0) {
+      consumer_sync<NW>();  // previous unit's merge buffers and q~ are free
+      transform_query(k);
+      consumer_sync<NW>();
     }
-    consumer_sync<NW>();
     // B operands of the score mma: k-step kk, rows {2c, 2c+1, 2c+8, 2c+9} hold
     // dims 32c + 4kk + {0, 1, 2, 3}; column = r (G <= 4: head r / 2, hi part
     // for even r, lo for odd r; G > 4: head r, hi in qa and lo in qb).
@@ -849,42 +851,38 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       l_run[gi] = 0.f;
     }
     if (k == 0) pdl_wait();  // partials are written only after the previous kernel completes
+    pb[0][0] = pb[0][1] = pb[1][0] = pb[1][1] = 0u;  // nothing pending yet
 #pragma unroll
-    for (int nn = 0; nn < kNCH; ++nn) {  // nothing pending yet
-      pb[nn][0][0] = pb[nn][0][1] = pb[nn][1][0] = pb[nn][1][1] = 0u;
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) pvc[nn][jj] = VCodes<DV, BV>{};
-    }
+    for (int jj = 0; jj < 4; ++jj) pvc[jj] = VCodes<DV, BV>{};
 
     for (int j = 0; j < u.count; ++j) {
-      bool ok = !*abort_flag && mbar_wait_bounded(full + slot, phase, abort_flag, p.timeout_ns);
-      ok = __all_sync(kFull, ok);
-      if (!ok && lane == 0 && !*abort_flag) {
-        *abort_flag = 1;
-        report(p.status, kDevTimeout);
+      bool ok = mbar_try_wait(full + slot, phase);
+      if (!__all_sync(kFull, ok)) {  // slow path: bounded wait
+        ok = !*abort_flag && mbar_wait_bounded(full + slot, phase, abort_flag, p.timeout_ns);
+        ok = __all_sync(kFull, ok);
+        if (!ok && lane == 0 && !*abort_flag) {
+          *abort_flag = 1;
+          report(p.status, kDevTimeout);
+        }
       }
       const int4 m = meta[slot];
-      const int off = warp * kSlice;             // slice offset inside the stage
-      const int tok0 = m.x + off;                // first token of the slice
-      const uint32_t bits = (static_cast<uint32_t>(m.z) >> (kNCH * warp)) & ((1u << kNCH) - 1u);
-      load_codes(stages + static_cast<size_t>(slot) * stage_bytes, off);
+      const int tok0 = m.x + warp * kChunk;      // first token of the warp's chunk
+      const bool live = ok && ((static_cast<uint32_t>(m.z) >> warp) & 1u) && tok0 < m.y;
+      load_codes(stages + slot * kStageBytes);
       __syncwarp();
       if (lane == 0) mbar_arrive(empty + slot);  // codes are in registers: the slot may be refilled
       if (++slot == NS) {
         slot = 0;
         phase ^= 1u;
       }
-      float sc[kNCH][4];
+      float sc[4];
       fused(sc, true);                           // scores now, P.V of the previous stage
-      // tokens past the end, and chunks whose page was invalid, get p = 0
-      softmax(sc, tok0, m.y, (ok && tok0 < m.y) ? bits : 0u);
+      softmax(sc, tok0, m.y, live);              // tokens past the end and invalid pages: p = 0
 #pragma unroll
-      for (int nn = 0; nn < kNCH; ++nn)
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) pvc[nn][jj] = vc[nn][jj];
+      for (int jj = 0; jj < 4; ++jj) pvc[jj] = vc[jj];
     }
     {  // P.V of the unit's last stage
-      float sc[kNCH][4];
+      float sc[4];
       fused(sc, false);
     }
 
@@ -916,33 +914,39 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       }
     }
     consumer_sync<NW>();
-    for (int i = tid; i < G * kHeadDim; i += kConsumerThreads) {
-      const int g = i / kHeadDim, d = i % kHeadDim;
+    // one thread per 4 output dims of a head: o = sum_w 2^(m_w - M) o_w, l likewise
+    for (int i = tid; i < G * (kHeadDim / 4); i += kConsumerThreads) {
+      const int g = i / (kHeadDim / 4), d4 = i % (kHeadDim / 4);
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < NW; ++w) M = fmaxf(M, mlbuf[w * G + g].x);
-      float o = 0.f, l = 0.f;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      float l = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
           const float2 ml = mlbuf[w * G + g];
           const float f = fast_exp2(ml.x - M);
-          o = fmaf(f, merge[(w * G + g) * kHeadDim + d], o);
+          const float4 v = reinterpret_cast<const float4*>(merge + (w * G + g) * kHeadDim)[d4];
+          o.x = fmaf(f, v.x, o.x);
+          o.y = fmaf(f, v.y, o.y);
+          o.z = fmaf(f, v.z, o.z);
+          o.w = fmaf(f, v.w, o.w);
           l = fmaf(f, ml.y, l);
         }
       }
       const long long row = (static_cast<long long>(u.b) * p.hq + u.kvh * G + g) * p.splits + u.s;
-      p.ws_o[row * kHeadDim + d] = o;
-      if (d == 0) p.ws_ml[row] = make_float2(M, l);
+      reinterpret_cast<float4*>(p.ws_o + row * kHeadDim)[d4] = o;
+      if (d4 == 0) p.ws_ml[row] = make_float2(M, l);
     }
   }
   __syncthreads();  // matches the producers' final barrier
 }
 
-template <int DK, int BK, int DV, int BV, int NG, int NW, int NCH>
+template <int DK, int BK, int DV, int BV, int NG, int NW>
 cudaError_t launch_split(const DecodeParams& p, int grid, size_t smem, cudaStream_t stream,
                          bool overlap) {
-  auto kern = vq_decode_split_kernel<DK, BK, DV, BV, NG, NW, NCH>;
+  auto kern = vq_decode_split_kernel<DK, BK, DV, BV, NG, NW>;
   static SmemOptIn opt_in;
   cudaError_t e = ensure_smem(kern, smem, opt_in);
   if (e != cudaSuccess) return e;
@@ -954,15 +958,12 @@ template <int DK, int BK, int DV, int BV>
 cudaError_t launch_formats(const DecodeParams& p, int grid, size_t smem, cudaStream_t stream,
                            bool ov) {
   const bool wide = p.group > 4;
-  if (p.warps == 12 && p.chunks == 1)
-    return wide ? launch_split<DK, BK, DV, BV, 8, 12, 1>(p, grid, smem, stream, ov)
-                : launch_split<DK, BK, DV, BV, 4, 12, 1>(p, grid, smem, stream, ov);
-  if (p.warps == 8 && p.chunks == 2)
-    return wide ? launch_split<DK, BK, DV, BV, 8, 8, 2>(p, grid, smem, stream, ov)
-                : launch_split<DK, BK, DV, BV, 4, 8, 2>(p, grid, smem, stream, ov);
-  if (p.warps == 8 && p.chunks == 1)
-    return wide ? launch_split<DK, BK, DV, BV, 8, 8, 1>(p, grid, smem, stream, ov)
-                : launch_split<DK, BK, DV, BV, 4, 8, 1>(p, grid, smem, stream, ov);
+  if (p.warps == 12)
+    return wide ? launch_split<DK, BK, DV, BV, 8, 12>(p, grid, smem, stream, ov)
+                : launch_split<DK, BK, DV, BV, 4, 12>(p, grid, smem, stream, ov);
+  if (p.warps == 8)
+    return wide ? launch_split<DK, BK, DV, BV, 8, 8>(p, grid, smem, stream, ov)
+                : launch_split<DK, BK, DV, BV, 4, 8>(p, grid, smem, stream, ov);
   return cudaErrorInvalidValue;
 }
 

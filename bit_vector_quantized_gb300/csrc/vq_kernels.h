@@ -56,7 +56,7 @@ struct DecodeParams {
   int split_q, split_r;       // ceil(max_seq_len / 32) = split_q * splits + split_r
   int k_row, v_row;
   int nstage;
-  int warps, chunks;          // consumer shape (DecodeShape)
+  int warps;                  // consumer warps (DecodeShape)
   float qscale;               // softmax scale * log2(e) / sqrt(128)
 };
 
@@ -101,11 +101,13 @@ constexpr int kProducerWarps = 4;  // TMA-issuing warps (one in four stages each
 constexpr int kMaxUnitsPerCta = 256;
 constexpr int kUnitTok = 32;       // split boundaries are multiples of this many tokens
 
-// Consumer shape: `warps` consumer warps, each taking `chunks` 16-token mma
-// chunks of every pipeline stage (a stage holds warps * chunks * 16 tokens).
+constexpr int kMaxStages = 16;     // pipeline slots of the split kernel, at most
+
+// Consumer shape: `warps` consumer warps, each taking one 16-token mma chunk
+// of every pipeline stage (a stage holds warps * 16 tokens).
 struct DecodeShape {
-  int warps, chunks;
-  __host__ __device__ int stage_tok() const { return warps * chunks * 16; }
+  int warps;
+  __host__ __device__ int stage_tok() const { return warps * 16; }
 };
 
 // Shared-memory carve-up of the split attention kernel (bytes, 128-aligned);
