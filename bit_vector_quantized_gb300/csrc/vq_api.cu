@@ -301,7 +301,7 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
                          int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t max_seq_len,
                          float softmax_scale, int32_t num_splits, const void* workspace,
                          size_t workspace_bytes, int32_t* status, vqk::DecodeParams& p,
-                         int& grid, size_t& smem) {
+                         int& grid, size_t& smem, bool* append = nullptr) {
   const vq_layout& L = *layout;
   const void* ptrs[] = {q, lambda, codebook_k, codebook_v, k_pool, v_pool, page_table, seq_lens, workspace};
   const char* names[] = {"q", "lambda", "codebook_k", "codebook_v", "k_pool", "v_pool",
@@ -369,11 +369,14 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
   // apart only; with at least as many stages as producer warps, the
   // producer's own previous stage guarantees the barrier is at most one phase
   // behind.
+  bool with_append = false;
   auto stages_for = [&](const vqk::DecodeShape& sh, size_t& bytes) {
     int ns = vqk::kMaxStages;
     for (; ns >= vqk::kProducerWarps; --ns) {
       bytes = vqk::decode_smem(L.k_bits, L.v_bits, p.group, p.k_row, p.v_row, ns, sh.warps,
-                               sh.stage_tok()).total;
+                               sh.stage_tok(), with_append ? vqk::append_enc_bytes(L.k_bits, L.v_bits) : 0,
+                               with_append ? vqk::append_scratch_bytes(sh.warps, L.k_sub, L.v_sub) : 0)
+                  .total;
       if (optin <= 0 || bytes <= static_cast<size_t>(optin)) return ns;
     }
     return 0;
@@ -398,6 +401,20 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
                 "decode pipeline does not fit: %d consumer warps need %zu bytes of shared memory "
                 "for %d stages",
                 shape.warps, smem, vqk::kProducerWarps);
+  // The decode-step append inside the attention kernel needs a little more
+  // shared memory; it runs only with the same consumer shape (so the results
+  // equal the separate append and attention bit for bit) and enough stages.
+  if (append && *append) {
+    with_append = true;
+    size_t bytes_app = 0;
+    const int ns_app = stages_for(shape, bytes_app);
+    if (ns_app >= vqk::kProducerWarps) {
+      nstage = ns_app;
+      smem = bytes_app;
+    } else {
+      *append = false;
+    }
+  }
   p.warps = shape.warps;
   p.nstage = nstage;
   return VQ_OK;
@@ -520,10 +537,32 @@ vq_status vq_decode_step(const vq_layout* layout, int32_t batch, const void* q, 
   vqk::DecodeParams p;
   int grid = 0;
   size_t smem = 0;
+  // Formats with byte-aligned K codes encode the new token inside the
+  // attention kernel (one launch, then the merge) when the attention kernel's
+  // shape leaves room for it; the 1.5-bit format appends with the encode
+  // kernel first.
+  // One CTA encodes each appended token in its prologue, so the fusion pays
+  // off while there is about one append per CTA; with more, the separate
+  // encode kernel spreads them over the GPU sooner (measured: 32K, ragged
+  // batch-16 and 196K steps faster fused, the batch-64 step slower).
+  const int sms_now = device_sms();
+  bool fused = L.k_bits <= 9 && L.v_bits <= 9 &&
+               static_cast<long long>(batch) * L.num_kv_heads <= (sms_now > 0 ? sms_now : 0);
   st = prepare_decode(layout, batch, q, lambda, codebook_k, codebook_v, k_pool, v_pool, num_pages,
                       page_table, max_pages_per_seq, seq_lens, max_seq_len, softmax_scale,
-                      num_splits, workspace, workspace_bytes, status, p, grid, smem);
+                      num_splits, workspace, workspace_bytes, status, p, grid, smem, &fused);
   if (st != VQ_OK) return st;
+  if (fused) {
+    p.append = 1;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_pool_w = static_cast<uint8_t*>(k_pool);
+    p.v_pool_w = static_cast<uint8_t*>(v_pool);
+    st = launch_partial(L, p, grid, smem, stream, false);
+    if (st != VQ_OK) return st;
+    return combine_impl(layout, batch, max_seq_len, p.splits, workspace, workspace_bytes, out, stream,
+                        true);
+  }
 
   // 1. append: token seq_lens[b] - 1 of every sequence, slot from the page table
   vqk::EncodeParams ep{};

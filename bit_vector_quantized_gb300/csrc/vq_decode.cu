@@ -195,11 +195,19 @@ struct UnitId {
   int b, kvh, s;
 };
 
+// Unit u of the grid goes to CTA u % grid and is (split, sequence, KV head)
+// with the split index varying slowest: the CTAs each get a mix of splits,
+// and with them an even share of the decode-step appends (the unit holding a
+// sequence's last token encodes it).  Measured against the split-fastest
+// order: ~5 % faster on the long-context shapes, ~3 % slower at batch 64 with
+// two splits; an order chosen at run time cost more than either (the kernel's
+// instruction count rose 15 %).
 __device__ __forceinline__ UnitId unit_id(const DecodeParams& p, int k) {
   const int u = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+  const int pairs = p.batch * p.hkv;
   UnitId id;
-  id.s = u % p.splits;
-  const int bk = u / p.splits;
+  id.s = u / pairs;
+  const int bk = u - id.s * pairs;
   id.kvh = bk % p.hkv;
   id.b = bk / p.hkv;
   return id;
@@ -246,6 +254,25 @@ __device__ __forceinline__ UnitStages unit_stages(const DecodeParams& p, int k, 
   return u;
 }
 
+// Decode-step append inside the attention kernel: the new token of (b, kvh)
+// is token raw_len - 1 (raw_len = seq_lens[b], unclamped).  The unit whose
+// split holds that position encodes and stores it, and so does the last
+// split when the position is at or past max_seq_len (stored, not attended).
+__device__ __forceinline__ bool append_owned(const DecodeParams& p, int s, int raw_len) {
+  if (raw_len < 1) return false;
+  const int pos = raw_len - 1;
+  const int a = split_first_block(p, s);
+  const int te = min((a + p.split_q + (s < p.split_r ? 1 : 0)) * kUnitTok, p.max_seq_len);
+  return (pos >= a * kUnitTok && pos < te) || (s == p.splits - 1 && pos >= p.max_seq_len);
+}
+
+// True when the appended token is attended in unit u: a stage of the unit
+// then copies its rows, which must be in the pools first.
+__device__ __forceinline__ bool append_attended(const DecodeParams& p, int t_begin, int t_end, int raw_len) {
+  const int pos = raw_len - 1;
+  return raw_len >= 1 && raw_len <= p.max_seq_len && pos >= t_begin && pos < t_end;
+}
+
 // Packed code-row bytes of a format: (128 / d) codes of b bits, rounded up to 4 bytes.
 template <int D, int B>
 struct RowBytes {
@@ -269,7 +296,112 @@ __device__ __forceinline__ int piece_lo(int t0, int lane, int l2) {
   return max(t0, ((t0 >> l2) + (lane & 15)) << l2);
 }
 
-template <int DK, int BK, int DV, int BV, int NG, int NW>
+// ---- decode-step append inside the attention kernel ---------------------------
+// Nearest centroid over [j0, j1) for the lane's sub-vectors of a 128-vector
+// held 4 elements per lane (d = 4: sub-vector `lane`; d = 2: sub-vectors
+// 2 lane and 2 lane + 1).  The score ||c||^2 - 2 x.c is formed as the encode
+// kernel forms it (the same fused multiply-adds, in the same order, on the same
+// fp32 -2 c and ||c||^2 values), and a strict '<' in index order keeps the
+// lowest index among equal scores, so the codes are those of vq_encode_kv.
+template <int D>
+__device__ __forceinline__ void append_scan(const float (&x)[4], uint32_t half, const float* cn,
+                                            int j0, int j1, float (&best)[2], int (&idx)[2]) {
+  // centroid j: replica 0 of its table row (fp16); -2 c is exact in fp32
+  best[0] = best[1] = INFINITY;
+  idx[0] = idx[1] = 0x7fffffff;
+  if constexpr (D == 4) {
+    auto score = [&](int j) {
+      const uint2 w = tab64((static_cast<uint32_t>(j) << 8) | half);
+      const __half2 c01 = *reinterpret_cast<const __half2*>(&w.x), c23 = *reinterpret_cast<const __half2*>(&w.y);
+      float sc = cn[j];
+      sc = fmaf(x[0], -2.f * __low2float(c01), sc);
+      sc = fmaf(x[1], -2.f * __high2float(c01), sc);
+      sc = fmaf(x[2], -2.f * __low2float(c23), sc);
+      return fmaf(x[3], -2.f * __high2float(c23), sc);
+    };
+    int j = j0;
+    for (; j + 4 <= j1; j += 4) {
+      float sc[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) sc[u] = score(j + u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (sc[u] < best[0]) {
+          best[0] = sc[u];
+          idx[0] = j + u;
+        }
+    }
+    for (; j < j1; ++j) {
+      const float sc = score(j);
+      if (sc < best[0]) {
+        best[0] = sc;
+        idx[0] = j;
+      }
+    }
+  } else {
+    static_assert(D == 2, "sub-vector length 2 or 4");
+    for (int j = j0; j < j1; ++j) {
+      const uint32_t w = tab32((static_cast<uint32_t>(j) << 8) | half);
+      const __half2 c01 = *reinterpret_cast<const __half2*>(&w);
+      const float cx = -2.f * __low2float(c01), cy = -2.f * __high2float(c01);
+      const float n = cn[j];
+      const float s0 = fmaf(x[1], cy, fmaf(x[0], cx, n));
+      const float s1 = fmaf(x[3], cy, fmaf(x[2], cx, n));
+      if (s0 < best[0]) {
+        best[0] = s0;
+        idx[0] = j;
+      }
+      if (s1 < best[1]) {
+        best[1] = s1;
+        idx[1] = j;
+      }
+    }
+  }
+}
+
+// Merges the warps' argmin slices of one tensor, held as (score bits, index)
+// pairs [warp][lane][NS]: slices cover increasing index ranges, so a strict
+// '<' in warp order keeps the lowest index among equal scores.
+template <int NS>
+__device__ __forceinline__ void merge_slices(const int2* scr, int nw, int lane, int (&idx)[2]) {
+  float best[2] = {INFINITY, INFINITY};
+  idx[0] = idx[1] = 0x7fffffff;
+  for (int w = 0; w < nw; ++w)
+#pragma unroll
+    for (int t = 0; t < NS; ++t) {
+      const int2 e = scr[(w * 32 + lane) * NS + t];
+      if (__int_as_float(e.x) < best[t]) {
+        best[t] = __int_as_float(e.x);
+        idx[t] = e.y;
+      }
+    }
+}
+
+// Word `lane` of a packed code row: code i (sub-vector i, held in register
+// i % NS of lane i / NS) occupies bits [i BITS, (i + 1) BITS) of the LSB-first
+// stream.  Every lane of the warp must call it (shuffles).
+template <int NS, int BITS>
+__device__ __forceinline__ uint32_t pack_row_word(const int (&idx)[2], int lane) {
+  constexpr int S = 32 * NS;  // codes in the row
+  const int i_lo = (32 * lane) / BITS;
+  uint32_t word = 0;
+#pragma unroll
+  for (int k = 0; k < 32 / BITS + 2; ++k) {
+    const int i = i_lo + k;
+    const int own = min(i / NS, 31);
+    uint32_t v = __shfl_sync(kFull, static_cast<uint32_t>(idx[0]), own);
+    if constexpr (NS == 2) {
+      const uint32_t v1 = __shfl_sync(kFull, static_cast<uint32_t>(idx[1]), own);
+      v = (i & 1) ? v1 : v;
+    }
+    const int pos = i * BITS - 32 * lane;
+    if (i < S && pos < 32 && pos > -BITS)
+      word |= static_cast<uint32_t>((static_cast<uint64_t>(v) << (pos + 32)) >> 32);
+  }
+  return word;
+}
+
+template <int DK, int BK, int DV, int BV, int NG, int NW, bool kAppend>
 __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split_kernel(const DecodeParams p) {
   static_assert(BK == 8 || (DK == 8 && BK == 12 && DV == 8 && BV == 12),
                 "K codes are byte-aligned, or the 1.5-bit format (d = 8, 12-bit codes)");
@@ -284,7 +416,10 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   uint8_t* const smem = g_smem;
   const int G = p.group;
   const int NS = p.nstage;
-  const DecodeSmem L = decode_smem(BK, BV, G, KROW, VROW, NS, NW, kStageTok);
+  static_assert(!kAppend || !kWide, "the 1.5-bit format appends with the encode kernel");
+  const DecodeSmem L = decode_smem(BK, BV, G, KROW, VROW, NS, NW, kStageTok,
+                                   kAppend ? append_enc_bytes(BK, BV) : 0,
+                                   kAppend ? append_scratch_bytes(NW, DK, DV) : 0);
   float* qt = reinterpret_cast<float*>(smem + L.qt);
   float* merge = reinterpret_cast<float*>(smem + L.merge);
   float2* mlbuf = reinterpret_cast<float2*>(smem + L.ml);
@@ -293,6 +428,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   int4* meta = reinterpret_cast<int4*>(smem + L.meta);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar);
   uint64_t* empty = full + NS;
+  uint64_t* app_bar = full + 2 * NS;  // fused append: the encoded rows are in the pools
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flag);
   uint8_t* stages = smem + L.stage;
 
@@ -370,6 +506,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       mbar_init(full + i, 1);
       mbar_init(empty + i, NW);
     }
+    mbar_init(app_bar, 2);  // consumer warps 0 (K rows) and 1 (V rows)
     mbar_init_fence();
     *abort_flag = 0;
   }
@@ -389,7 +526,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int k = ptid + i * NP * 32;
-      if (k < n_units) ulen_p[k] = clamp_len(len_r[i]);
+      if (k < n_units) ulen_p[k] = len_r[i];  // raw: the append needs the unclamped length
     }
     producer_sync<NP>();
     const int P = p.page_size;
@@ -403,7 +540,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       while (it.k < n_units && it.j >= it.u.count) {
         ++it.k;
         it.j = 0;
-        if (it.k < n_units) it.u = unit_stages<kStageTok>(p, it.k, ulen_p[it.k]);
+        if (it.k < n_units) it.u = unit_stages<kStageTok>(p, it.k, clamp_len(ulen_p[it.k]));
       }
     };
     auto skip = [&](It& it) {  // advance by NP stages
@@ -453,7 +590,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
     It cur;
     cur.k = 0;
     cur.j = 0;
-    if (n_units > 0) cur.u = unit_stages<kStageTok>(p, 0, ulen_p[0]);
+    if (n_units > 0) cur.u = unit_stages<kStageTok>(p, 0, clamp_len(ulen_p[0]));
     it_seek(cur);
 #pragma unroll 1
     for (int i = 0; i < pw && cur.k < n_units; ++i) {
@@ -464,7 +601,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
     int page = (cur.k == 0 && cur.j == pw) ? page_r : lookup(cur);
     pdl_wait();  // the pools may be written by the previous kernel: copy only after it
     int n = pw;
-    bool stop = false;
+    bool stop = false, app_ready = false;
     while (cur.k < n_units) {
       const int slot = n % NS;
       if (n >= NS) {  // wait until the consumers have released the slot
@@ -480,6 +617,25 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
             stop = true;
             break;
           }
+        }
+      }
+      if (kAppend && !app_ready) {  // the stage holding an appended token waits for its rows
+        const int raw = ulen_p[cur.k];
+        const int t0 = cur.u.t_begin + cur.j * kStageTok;
+        if (append_attended(p, t0, min(t0 + kStageTok, cur.u.t_end), raw)) {
+          bool ok = mbar_try_wait(app_bar, 0u);
+          if (!__all_sync(kFull, ok)) {
+            ok = !*abort_flag && mbar_wait_bounded(app_bar, 0u, abort_flag, p.timeout_ns);
+            if (!__all_sync(kFull, ok)) {
+              if (lane == 0 && !*abort_flag) {
+                *abort_flag = 1;
+                report(p.status, kDevTimeout);
+              }
+              stop = true;
+              break;
+            }
+          }
+          app_ready = true;
         }
       }
       issue(cur.u, cur.j, page, n);
@@ -562,8 +718,31 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
     fill(cbk_r, kNK, 1 << BK, DK, 0u);
     fill(cbv_r, kNV, 1 << BV, DV, 128u);
   }
-  if (tid < n_units) ulen_c[tid] = clamp_len(len_r[0]);
+  if (tid < n_units) ulen_c[tid] = len_r[0];  // raw: the append needs the unclamped length
 
+  // Fused append: ||c||^2 of every centroid in fp32, computed as the encode
+  // kernel computes it (a chain of fused multiply-adds in element order).
+  float* const enc_kn = reinterpret_cast<float*>(smem + L.enc);
+  float* const enc_vn = enc_kn + (1 << BK);
+  if constexpr (kAppend) {
+    {
+      auto norms = [&](const uint2 (&cb)[kNB], int n_i, int rows, int d, float* cn) {
+#pragma unroll
+        for (int i = 0; i < kNB; ++i) {
+          const int j = tid + i * kConsumerThreads;
+          if (i >= n_i || j >= rows) break;
+          const __half2 h01 = *reinterpret_cast<const __half2*>(&cb[i].x);
+          const __half2 h23 = *reinterpret_cast<const __half2*>(&cb[i].y);
+          const float v[4] = {__low2float(h01), __high2float(h01), __low2float(h23), __high2float(h23)};
+          float n = 0.f;
+          for (int e = 0; e < d; ++e) n = fmaf(v[e], v[e], n);
+          cn[j] = n;
+        }
+      };
+      norms(cbk_r, kNK, 1 << BK, DK, enc_kn);
+      norms(cbv_r, kNV, 1 << BV, DV, enc_vn);
+    }
+  }
   // q~ = q diag(lambda) H_D * scale * log2(e), split into fp16 hi + lo parts
   // and stored in the score mma's B-operand order: table [head][hi, lo][c][16
   // words], words 2kk, 2kk+1 = dims 32c + 4kk + {0, 1} and {2, 3} (lane l of
@@ -588,6 +767,89 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       *reinterpret_cast<uint2*>(qf + 4 * 16) = make_uint2(l01, l23);
     }
   };
+  // Fused append: encodes the new token of unit u's (sequence, KV head)
+  // (append_owned).  Every consumer warp scans a slice of each codebook;
+  // warps 0 and 1 merge the slices in index order, pack the K and V rows and
+  // store them into the pools through the page table, each storing lane
+  // fencing its stores for the copy engine (the bulk copies that read them
+  // are issued after the caller's signal on app_bar).
+  auto append_encode = [&](const UnitStages& u, int raw_len) {
+    if constexpr (kAppend) {
+      const int pos = raw_len - 1;
+      constexpr int NSK = DK == 2 ? 2 : 1, NSV = DV == 2 ? 2 : 1;
+      const long long vrow = (static_cast<long long>(u.b) * p.hkv + u.kvh) * kHeadDim;
+      const uint2 rk = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.k_new) + vrow) + lane);
+      const uint2 rv = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.v_new) + vrow) + lane);
+      const float4 lam = __ldg(reinterpret_cast<const float4*>(p.lambda + u.kvh * kHeadDim) + lane);
+      const int pi = pos / p.page_size;
+      const int page = pi < p.max_pages ? __ldg(p.page_table + static_cast<long long>(u.b) * p.max_pages + pi) : -1;
+      float xk[4], xv[4];
+      {
+        const __half2 k01 = *reinterpret_cast<const __half2*>(&rk.x), k23 = *reinterpret_cast<const __half2*>(&rk.y);
+        const __half2 v01 = *reinterpret_cast<const __half2*>(&rv.x), v23 = *reinterpret_cast<const __half2*>(&rv.y);
+        xk[0] = __low2float(k01) / lam.x;  // keys: smoothing, Walsh-Hadamard, 1/sqrt(128)
+        xk[1] = __high2float(k01) / lam.y;
+        xk[2] = __low2float(k23) / lam.z;
+        xk[3] = __high2float(k23) / lam.w;
+        xv[0] = __low2float(v01);
+        xv[1] = __high2float(v01);
+        xv[2] = __low2float(v23);
+        xv[3] = __high2float(v23);
+      }
+      fwht128_warp(xk, lane);
+      const float rs = 0.08838834764831845f;  // 1/sqrt(128)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) xk[e] *= rs;
+      float bk[2], bv[2];
+      int ik[2], iv[2];
+      append_scan<DK>(xk, 0u, enc_kn, (warp << BK) / NW, ((warp + 1) << BK) / NW, bk, ik);
+      append_scan<DV>(xv, 128u, enc_vn, (warp << BV) / NW, ((warp + 1) << BV) / NW, bv, iv);
+      // scratch: K entries [warp][lane][NSK], then V entries [warp][lane][NSV] (score bits, index)
+      int2* scr_k = reinterpret_cast<int2*>(merge);
+      int2* scr_v = scr_k + NW * 32 * NSK;
+#pragma unroll
+      for (int t = 0; t < NSK; ++t) scr_k[(warp * 32 + lane) * NSK + t] = make_int2(__float_as_int(bk[t]), ik[t]);
+#pragma unroll
+      for (int t = 0; t < NSV; ++t) scr_v[(warp * 32 + lane) * NSV + t] = make_int2(__float_as_int(bv[t]), iv[t]);
+      consumer_sync<NW>();
+      if (warp < 2) {  // warp 0 merges and stores K, warp 1 V
+        const int tv = warp;
+        int idx[2];
+        if (tv == 0) merge_slices<NSK>(scr_k, NW, lane, idx);
+        else merge_slices<NSV>(scr_v, NW, lane, idx);
+        const uint32_t word = tv == 0 ? pack_row_word<NSK, BK>(idx, lane) : pack_row_word<NSV, BV>(idx, lane);
+        const int row = tv == 0 ? KROW : VROW;
+        const bool ok = page >= 0 && page < p.num_pages;
+        if (!ok && lane == 0 && tv == 0) report(p.status, kDevBadPage);
+        if (ok && lane < row / 4) {
+          pdl_wait();  // no-op: this kernel is the first of its call
+          uint8_t* pool = tv == 0 ? p.k_pool_w : p.v_pool_w;
+          const long long r0 = (static_cast<long long>(page) * p.hkv + u.kvh) * p.page_size + pos % p.page_size;
+          reinterpret_cast<uint32_t*>(pool + r0 * row)[lane] = word;
+          fence_proxy_async_global();
+        }
+      }
+    }
+  };
+  if constexpr (kAppend) {  // every appended token of the CTA's units, before the first unit starts
+    consumer_sync<NW>();  // ||c||^2 tables visible
+    bool any = false, attended = false;
+    for (int k = 0; k < n_units; ++k) {
+      const int raw = ulen_c[k];
+      const UnitId id = unit_id(p, k);
+      if (!append_owned(p, id.s, raw)) continue;
+      if (any) consumer_sync<NW>();  // the previous encode's scratch has been read
+      const UnitStages u = unit_stages<kStageTok>(p, k, clamp_len(raw));
+      append_encode(u, raw);
+      any = true;
+      attended = attended || append_attended(p, u.t_begin, u.t_end, raw);
+    }
+    if (attended && warp < 2) {  // the rows of the attended appends are in the pools
+      __syncwarp();
+      if (lane == 0) mbar_arrive(app_bar);
+    }
+    consumer_sync<NW>();  // the merge buffer (the encode scratch) is free again
+  }
   transform_query(0);
   consumer_sync<NW>();  // codebook table, unit lengths and the first unit's q~ visible
 
@@ -804,9 +1066,9 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   int slot = 0;          // slot of the next stage (stages run in the producers' order)
   uint32_t phase = 0u;   // parity of the slot's current fill
   for (int k = 0; k < n_units; ++k) {
-    const UnitStages u = unit_stages<kStageTok>(p, k, ulen_c[k]);
+    const UnitStages u = unit_stages<kStageTok>(p, k, clamp_len(ulen_c[k]));
+    if (k > 0) consumer_sync<NW>();  // previous unit's merge buffers and q~ are free
     if (k > 0) {
-      consumer_sync<NW>();  // previous unit's merge buffers and q~ are free
       transform_query(k);
       consumer_sync<NW>();
     }
@@ -943,10 +1205,10 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   __syncthreads();  // matches the producers' final barrier
 }
 
-template <int DK, int BK, int DV, int BV, int NG, int NW>
+template <int DK, int BK, int DV, int BV, int NG, int NW, bool kAppend>
 cudaError_t launch_split(const DecodeParams& p, int grid, size_t smem, cudaStream_t stream,
                          bool overlap) {
-  auto kern = vq_decode_split_kernel<DK, BK, DV, BV, NG, NW>;
+  auto kern = vq_decode_split_kernel<DK, BK, DV, BV, NG, NW, kAppend>;
   static SmemOptIn opt_in;
   cudaError_t e = ensure_smem(kern, smem, opt_in);
   if (e != cudaSuccess) return e;
@@ -958,12 +1220,21 @@ template <int DK, int BK, int DV, int BV>
 cudaError_t launch_formats(const DecodeParams& p, int grid, size_t smem, cudaStream_t stream,
                            bool ov) {
   const bool wide = p.group > 4;
+  if (p.append) {  // the decode step with the append inside: the default shapes only
+    if constexpr (BK <= 9 && BV <= 9) {
+      if (p.warps == 12 && !wide) return launch_split<DK, BK, DV, BV, 4, 12, true>(p, grid, smem, stream, ov);
+      if (p.warps == 8)
+        return wide ? launch_split<DK, BK, DV, BV, 8, 8, true>(p, grid, smem, stream, ov)
+                    : launch_split<DK, BK, DV, BV, 4, 8, true>(p, grid, smem, stream, ov);
+    }
+    return cudaErrorInvalidValue;
+  }
   if (p.warps == 12)
-    return wide ? launch_split<DK, BK, DV, BV, 8, 12>(p, grid, smem, stream, ov)
-                : launch_split<DK, BK, DV, BV, 4, 12>(p, grid, smem, stream, ov);
+    return wide ? launch_split<DK, BK, DV, BV, 8, 12, false>(p, grid, smem, stream, ov)
+                : launch_split<DK, BK, DV, BV, 4, 12, false>(p, grid, smem, stream, ov);
   if (p.warps == 8)
-    return wide ? launch_split<DK, BK, DV, BV, 8, 8>(p, grid, smem, stream, ov)
-                : launch_split<DK, BK, DV, BV, 4, 8>(p, grid, smem, stream, ov);
+    return wide ? launch_split<DK, BK, DV, BV, 8, 8, false>(p, grid, smem, stream, ov)
+                : launch_split<DK, BK, DV, BV, 4, 8, false>(p, grid, smem, stream, ov);
   return cudaErrorInvalidValue;
 }
 

@@ -113,10 +113,11 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
-// Orders this thread's earlier generic-proxy shared-memory accesses before
-// later async-proxy (bulk copy) accesses.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+// Orders this thread's earlier generic-proxy global-memory accesses before
+// later async-proxy (bulk copy) accesses, once a release / acquire pair has
+// carried them to the issuing thread.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // ------------------------------------------------------------ warp mma ---

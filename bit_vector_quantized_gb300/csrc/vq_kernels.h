@@ -58,6 +58,15 @@ struct DecodeParams {
   int nstage;
   int warps;                  // consumer warps (DecodeShape)
   float qscale;               // softmax scale * log2(e) / sqrt(128)
+  // Decode-step append inside the attention kernel (append != 0): the new
+  // token of every sequence, position seq_lens[b] - 1, is encoded by the CTA
+  // whose unit holds that position and written to the pools through the
+  // page table, and its codes join the attention directly.
+  int append;
+  const void* k_new;          // fp16 [B][Hkv][128]
+  const void* v_new;
+  uint8_t* k_pool_w;          // the pools, written (k_pool / v_pool as writable pointers)
+  uint8_t* v_pool_w;
 };
 
 struct DequantParams {
@@ -118,7 +127,7 @@ struct DecodeShape {
 // centroids of 8 elements) has no replicas: 32 bytes per centroid index, laid
 // out half-major ([tensor][half][code] x 8 bytes).
 struct DecodeSmem {
-  int tab, qt, merge, ml, units, meta, bar, flag, stage, total;
+  int tab, qt, merge, ml, units, meta, bar, flag, enc, stage, total;
 };
 
 constexpr int kTabRow = 256;      // bytes per codebook table row (replicated centroids)
@@ -126,19 +135,37 @@ constexpr int kTabRowWide = 32;   // 1.5-bit format (12-bit codes): K and V cent
 
 __host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
 
+// Bytes of the fused append's encode tables: per tensor ||c_j||^2 (fp32,
+// 2^bits); then the packed new K and V rows (64 bytes each, at most).  The
+// centroids themselves are read from the replicated fp16 table.
+__host__ __device__ inline int append_enc_bytes(int k_bits, int v_bits) {
+  return ((1 << k_bits) + (1 << v_bits)) * 4 + 128;
+}
+
+// Bytes of the fused append's argmin scratch: per tensor, warps x 32 lanes x
+// (sub-vectors per lane: 2 for d = 2, else 1) x (score, index); it shares the
+// merge buffer.
+__host__ __device__ inline int append_scratch_bytes(int warps, int k_sub, int v_sub) {
+  return warps * 32 * ((k_sub == 2 ? 2 : 1) + (v_sub == 2 ? 2 : 1)) * 8;
+}
+
+// append_enc / append_scratch: the fused append's table and scratch bytes (0: no append)
 __host__ __device__ inline DecodeSmem decode_smem(int k_bits, int v_bits, int group, int k_row,
-                                                  int v_row, int nstage, int warps, int stage_tok) {
+                                                  int v_row, int nstage, int warps, int stage_tok,
+                                                  int append_enc = 0, int append_scratch = 0) {
   DecodeSmem s;
   int o = 0;
   const int rows = 1 << (k_bits > v_bits ? k_bits : v_bits);
   s.tab = o; o = align128(o + rows * (k_bits == 12 ? kTabRowWide : kTabRow));
   s.qt = o; o = align128(o + (group > 4 ? 8 : 4) * 128 * 4);  // q~ operand table, 4 or 8 heads
-  s.merge = o; o = align128(o + warps * group * 128 * 4);
+  const int merge = warps * group * 128 * 4;
+  s.merge = o; o = align128(o + (merge > append_scratch ? merge : append_scratch));
   s.ml = o; o = align128(o + warps * group * 8);
   s.units = o; o = align128(o + 2 * kMaxUnitsPerCta * 4);  // consumer and producer copies
   s.meta = o; o = align128(o + nstage * 16);
-  s.bar = o; o = align128(o + nstage * 2 * 8);
+  s.bar = o; o = align128(o + (nstage * 2 + 1) * 8);  // full and empty per slot, then the append's
   s.flag = o; o = align128(o + 16);
+  s.enc = o; o = align128(o + append_enc);
   s.stage = o; o = align128(o + nstage * stage_tok * (k_row + v_row));
   s.total = o;
   return s;

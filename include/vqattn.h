@@ -254,10 +254,18 @@ vq_status vq_decode_combine(const vq_layout* layout, int32_t batch, int32_t max_
  * are encoded and appended, then the query attends over the quantized cache).
  * Exactly the results of vq_encode_kv of the new tokens followed by
  * vq_decode_attention with the same split count, without a slot mapping: the
- * slots come from the page table.  Three kernels on `stream` (append encode,
- * split attention, merge); the attention kernel starts while the append is
- * encoding, prepares its codebook tables, and waits for the append before it
- * reads the pools.
+ * slots come from the page table.  Two ways, chosen by the library and equal
+ * bit for bit:
+ *   - with at most one sequence-KV-head pair per SM and a format whose codes
+ *     are at most 9 bits (every format but the 1.5-bit one), the attention
+ *     kernel itself encodes each new token (the CTA whose split holds it
+ *     encodes it before its first stage and stores the codes; the stage that
+ *     holds the token is copied after the store), then the merge: two kernels
+ *     (the fused append of HACK's decode kernel and of VecInfer's 注意力机制中的
+ *     向量量化KV缓存, where the new code joins the cached ones);
+ *   - otherwise three kernels: the append encode, the split attention (it
+ *     starts while the append runs, prepares its tables, and waits for the
+ *     append before it reads the pools) and the merge.
  *   k_new, v_new fp16 [batch][Hkv][D]: the new token of every sequence.  It is
  *                token seq_lens[b] - 1 of sequence b and goes to slot
  *                page_table[b][t / P] * P + t % P of the pools

@@ -125,3 +125,30 @@ def test_step_large_batch():
     assert a.device_status() == 0 and b.device_status() == 0
     assert torch.equal(a.k_pool, b.k_pool) and torch.equal(a.v_pool, b.v_pool)
     assert np.array_equal(got, ref)
+
+
+def test_step_length_beyond_max_seq_len():
+    """A sequence longer than max_seq_len: its new token is stored where
+    vq_encode_kv stores it, but, like every token at or past max_seq_len, it is
+    not attended."""
+    import bit_vector_quantized_gb300 as vq
+    w = _workload((4, 8, 4, 8), 4, batch=3, context=700)
+    _, a, b = _pair(w)
+    lens = a.lens + 1
+    ml = int(lens.min())                                     # shorter than the other sequences
+    assert (lens > ml).any()
+    q = W.queries(w)
+    a.append()                                               # every sequence's token lens - 1
+    seq = torch.from_numpy(lens.astype(np.int32)).cuda()
+    qd = torch.from_numpy(q).cuda()
+    ref = vq.decode_attention(a.layout, qd, a.lam, a.ck, a.cv, a.k_pool, a.v_pool, a.page_table, seq,
+                              ml, num_splits=3, status=a.status)
+    pos = [int(n) - 1 for n in lens]
+    kn = torch.from_numpy(np.stack([W.kv_tokens(w, bb, "k", p, p + 1)[0] for bb, p in enumerate(pos)])).cuda()
+    vn = torch.from_numpy(np.stack([W.kv_tokens(w, bb, "v", p, p + 1)[0] for bb, p in enumerate(pos)])).cuda()
+    got = vq.decode_step(b.layout, qd, kn, vn, b.lam, b.ck, b.cv, b.k_pool, b.v_pool, b.page_table, seq,
+                         ml, num_splits=3, status=b.status)
+    torch.cuda.synchronize()
+    assert a.device_status() == 0 and b.device_status() == 0
+    assert torch.equal(a.k_pool, b.k_pool) and torch.equal(a.v_pool, b.v_pool)
+    assert torch.equal(got, ref)
