@@ -72,6 +72,11 @@ def parse():
                     help="skip the dense fp16 attention comparison (context only)")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip the long-context and large-batch split-kernel blocks")
+    ap.add_argument("--no-methods", action="store_true",
+                    help="skip the score / P.V method comparison (gather, LUT, bins)")
+    ap.add_argument("--methods-only", action="store_true",
+                    help="launch the split kernel three times per method on the workload and "
+                         "exit (a short program for an ncu capture of the three methods)")
     return ap.parse_args()
 
 
@@ -502,6 +507,66 @@ def split_kernel_block(torch, vq, wi, dev, steps, l2, hbm_peak):
     return res
 
 
+METHODS = {0: "gather", 1: "lut", 2: "bins"}
+
+
+def method_comparison(torch, vq, wi, dev, steps, l2, hbm_peak, only_launch=False):
+    """The split kernel with each of the pages' score / P.V methods
+    (vq_decode_partial_method): in-register centroid gathers on the tensor
+    cores (the library's), a per-query q~ x K-codebook lookup table for the
+    scores (VecInfer, 内核实现细节 - 融合内核), and P.V through per-code bins
+    (CommVQ, 降低计算复杂度).  Timed like the headline split kernel, over seeded
+    random code bytes (the work and traffic do not depend on code values)."""
+    w = W.WORKLOADS[wi]
+    if not (w.k_sub == 4 and w.k_bits == 8 and w.v_sub == 4 and w.v_bits == 8
+            and w.num_q_heads // w.num_kv_heads <= 4):
+        return {"skipped": "the table-based methods are built for d = 4, 8-bit codes, G <= 4"}
+    lam, ck, cv = load_calib(wi)
+    layout = vq.make_layout(w.head_dim, w.num_q_heads, w.num_kv_heads, w.k_sub, w.k_bits,
+                            w.v_sub, w.v_bits, w.page_size)
+    lens = (W.seq_lens(w) + 1).astype(np.int32)
+    B, num_pages = w.batch, W.num_pages(w)
+    step_bytes = code_bytes_per_step(w)
+    copies = 1 if only_launch else max(1, -(-2 * l2 // step_bytes))
+    gen = torch.Generator(device=dev).manual_seed(2000 + wi)
+    krow, vrow = layout_row_bytes(w, "k"), layout_row_bytes(w, "v")
+    pools = [(torch.randint(0, 256, (num_pages, w.num_kv_heads, w.page_size, krow), generator=gen,
+                            device=dev, dtype=torch.uint8),
+              torch.randint(0, 256, (num_pages, w.num_kv_heads, w.page_size, vrow), generator=gen,
+                            device=dev, dtype=torch.uint8)) for _ in range(copies)]
+    table_d = torch.from_numpy(W.page_table(w)).to(dev)
+    seq_d = torch.from_numpy(lens).to(dev)
+    max_len = int(lens.max())
+    q_d = torch.from_numpy(W.queries(w)).to(dev)
+    lam_d, ck_d, cv_d = (torch.from_numpy(x).to(dev) for x in (lam, ck, cv))
+    splits = vq.vq_default_num_splits(layout, B, max_len)
+    ws_bytes = vq.vq_decode_workspace_bytes(layout, B, max_len, splits)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    p = lambda t: t.data_ptr()  # noqa: E731
+    res = {"workload": w.name, "num_splits": splits, "codes": "seeded uniform random bytes"}
+    for method, name in METHODS.items():
+        def fn(i, method=method):
+            kp, vp = pools[i % copies]
+            vq.vq_decode_partial_method(layout, B, p(q_d), p(lam_d), p(ck_d), p(cv_d), p(kp), p(vp),
+                                        num_pages, p(table_d), table_d.shape[1], p(seq_d), max_len,
+                                        0.0, splits, method, p(ws), ws_bytes, p(status),
+                                        torch.cuda.current_stream().cuda_stream)
+        if only_launch:
+            for i in range(3):
+                fn(i)
+            torch.cuda.synchronize()
+            continue
+        ms = graph_ms(torch, dev, fn, steps)
+        gbs = step_bytes / (ms / 1e3) / 1e9
+        res[name] = {"split_kernel_us": ms * 1e3, "achieved_gbs": gbs, "frac": gbs / hbm_peak}
+    torch.cuda.synchronize()
+    res["device_status"] = int(status.item())
+    del pools, ws
+    torch.cuda.empty_cache()
+    return res
+
+
 def encode_report(w, tokens, ms, sms, clocks):
     """Prefill encode throughput and its roofline.  The encode is bound by the FP32
     pipe: a nearest-centroid scan spends d fused multiply-adds per centroid and
@@ -569,6 +634,12 @@ def main():
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.methods_only:
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        r = method_comparison(torch, vq, args.workload, dev, 3, l2, measured_hbm()[0], only_launch=True)
+        print(json.dumps({"methods_only": w.name, "device_status": r.get("device_status"),
+                          "skipped": r.get("skipped")}), flush=True)
+        return
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -823,6 +894,13 @@ def main():
         except Exception as exc:
             residual = {"skipped": f"{type(exc).__name__}: {exc}"[:200]}
 
+    methods = None
+    if world == 1 and not args.no_methods:
+        try:
+            methods = method_comparison(torch, vq, args.workload, dev, min(K, 200), l2, hbm_peak)
+        except Exception as exc:  # context: never fail the bench line on it
+            methods = {"skipped": f"{type(exc).__name__}: {exc}"[:200]}
+
     others = None
     if world == 1 and not args.no_other_workloads:
         others = []
@@ -866,6 +944,7 @@ def main():
             "unfused_comparison": unfused,
             "residual_window": residual,
             "other_workloads": others,
+            "methods": methods,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * K, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -33,7 +33,7 @@ VQ_DEV_OK, VQ_DEV_BAD_PAGE, VQ_DEV_BAD_SLOT, VQ_DEV_TIMEOUT, VQ_DEV_BAD_CONFIG =
 # every symbol include/vqattn.h declares
 EXPORTED = ("vq_code_row_bytes", "vq_check_layout", "vq_encode_kv", "vq_decode_workspace_bytes",
             "vq_default_num_splits", "vq_decode_attention", "vq_decode_partial",
-            "vq_decode_combine", "vq_decode_step", "vq_dequantize_kv",
+            "vq_decode_partial_method", "vq_decode_combine", "vq_decode_step", "vq_dequantize_kv",
             "vq_decode_residual_workspace_bytes", "vq_decode_attention_residual",
             "vq_decode_attention_static", "vq_static_scratch_bytes", "vq_last_error",
             "vq_version")
@@ -88,6 +88,8 @@ def lib() -> ctypes.CDLL:
                                           ctypes.c_float, I32, P, P, SZ, P, P]),
             "vq_decode_partial": (I32, [LP, I32, P, P, P, P, P, P, I64, P, I32, P, I32,
                                         ctypes.c_float, I32, P, SZ, P, P]),
+            "vq_decode_partial_method": (I32, [LP, I32, P, P, P, P, P, P, I64, P, I32, P, I32,
+                                               ctypes.c_float, I32, I32, P, SZ, P, P]),
             "vq_decode_combine": (I32, [LP, I32, I32, I32, P, SZ, P, P]),
             "vq_decode_step": (I32, [LP, I32, P, P, P, P, P, P, P, P, I64, P, I32, P, I32,
                                      ctypes.c_float, I32, P, P, SZ, P, P]),
@@ -188,6 +190,20 @@ def vq_decode_partial(layout, batch, q, lambda_, codebook_k, codebook_v, k_pool,
                                    num_pages, _ptr(page_table), max_pages_per_seq, _ptr(seq_lens),
                                    max_seq_len, float(softmax_scale), num_splits, _ptr(workspace),
                                    workspace_bytes, _ptr(status), _ptr(stream)))
+
+
+VQ_METHOD_GATHER, VQ_METHOD_LUT, VQ_METHOD_BINS = 0, 1, 2
+
+
+def vq_decode_partial_method(layout, batch, q, lambda_, codebook_k, codebook_v, k_pool, v_pool,
+                             num_pages, page_table, max_pages_per_seq, seq_lens, max_seq_len,
+                             softmax_scale, num_splits, method, workspace, workspace_bytes,
+                             status=None, stream=None) -> None:
+    _check(lib().vq_decode_partial_method(
+        ctypes.byref(layout), batch, _ptr(q), _ptr(lambda_), _ptr(codebook_k), _ptr(codebook_v),
+        _ptr(k_pool), _ptr(v_pool), num_pages, _ptr(page_table), max_pages_per_seq, _ptr(seq_lens),
+        max_seq_len, float(softmax_scale), num_splits, method, _ptr(workspace), workspace_bytes,
+        _ptr(status), _ptr(stream)))
 
 
 def vq_decode_combine(layout, batch, max_seq_len, num_splits, workspace, workspace_bytes, out,
@@ -365,6 +381,40 @@ def decode_attention(layout: vq_layout, q, lambda_, codebook_k, codebook_v, k_po
                         _dev_ptr(out, torch.float16, "out", (B, layout.num_q_heads, D)),
                         _dev_ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
                         _dev_ptr(status, torch.int32, "status", (1,)), _stream(stream))
+    return out
+
+
+def decode_attention_method(layout: vq_layout, q, lambda_, codebook_k, codebook_v, k_pool,
+                            v_pool, page_table, seq_lens, max_seq_len: int, method: int,
+                            out=None, workspace=None, softmax_scale: float = 0.0,
+                            num_splits: int = 0, status=None, stream=None):
+    """decode_attention with an explicit score / P.V method (vq_decode_partial_method,
+    then vq_decode_combine)."""
+    torch = _torch()
+    B = q.shape[0]
+    D = layout.head_dim
+    if out is None:
+        out = torch.empty((B, layout.num_q_heads, D), dtype=torch.float16, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(layout, B, max_seq_len, num_splits, q.device)
+    st = _stream(stream)
+    vq_decode_partial_method(layout, B,
+                             _dev_ptr(q, torch.float16, "q", (B, layout.num_q_heads, D)),
+                             _dev_ptr(lambda_, torch.float32, "lambda", (layout.num_kv_heads, D)),
+                             _dev_ptr(codebook_k, torch.float16, "codebook_k",
+                                      (1 << layout.k_bits, layout.k_sub)),
+                             _dev_ptr(codebook_v, torch.float16, "codebook_v",
+                                      (1 << layout.v_bits, layout.v_sub)),
+                             _dev_ptr(k_pool, torch.uint8, "k_pool"),
+                             _dev_ptr(v_pool, torch.uint8, "v_pool"), k_pool.shape[0],
+                             _dev_ptr(page_table, torch.int32, "page_table"), page_table.shape[1],
+                             _dev_ptr(seq_lens, torch.int32, "seq_lens", (B,)), max_seq_len,
+                             softmax_scale, num_splits, method,
+                             _dev_ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+                             _dev_ptr(status, torch.int32, "status", (1,)), st)
+    vq_decode_combine(layout, B, max_seq_len, num_splits,
+                      _dev_ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+                      _dev_ptr(out, torch.float16, "out", (B, layout.num_q_heads, D)), st)
     return out
 
 

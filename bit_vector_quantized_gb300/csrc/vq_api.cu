@@ -301,7 +301,8 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
                          int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t max_seq_len,
                          float softmax_scale, int32_t num_splits, const void* workspace,
                          size_t workspace_bytes, int32_t* status, vqk::DecodeParams& p,
-                         int& grid, size_t& smem, bool* append = nullptr) {
+                         int& grid, size_t& smem, bool* append = nullptr,
+                         int method = vqk::kMethodGather) {
   const vq_layout& L = *layout;
   const void* ptrs[] = {q, lambda, codebook_k, codebook_v, k_pool, v_pool, page_table, seq_lens, workspace};
   const char* names[] = {"q", "lambda", "codebook_k", "codebook_v", "k_pool", "v_pool",
@@ -375,7 +376,8 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
     for (; ns >= vqk::kProducerWarps; --ns) {
       bytes = vqk::decode_smem(L.k_bits, L.v_bits, p.group, p.k_row, p.v_row, ns, sh.warps,
                                sh.stage_tok(), with_append ? vqk::append_enc_bytes(L.k_bits, L.v_bits) : 0,
-                               with_append ? vqk::append_scratch_bytes(sh.warps, L.k_sub, L.v_sub) : 0)
+                               with_append ? vqk::append_scratch_bytes(sh.warps, L.k_sub, L.v_sub) : 0,
+                               method)
                   .total;
       if (optin <= 0 || bytes <= static_cast<size_t>(optin)) return ns;
     }
@@ -390,6 +392,14 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
   if (const char* env = std::getenv("VQ_DECODE_SHAPE")) {
     if (std::strcmp(env, "8x1") == 0) shape = vqk::DecodeShape{8}, explicit_shape = true;
     if (std::strcmp(env, "12x1") == 0) shape = vqk::DecodeShape{12}, explicit_shape = true;
+  }
+  if (method != vqk::kMethodGather) {
+    if (!(L.k_sub == 4 && L.k_bits == 8 && L.v_sub == 4 && L.v_bits == 8 && p.group <= 4))
+      return fail(VQ_ERR_UNSUPPORTED,
+                  "the LUT and bins methods are built for k_sub = v_sub = 4, 8-bit codes and "
+                  "num_q_heads / num_kv_heads <= 4");
+    shape = vqk::DecodeShape{12};
+    explicit_shape = true;
   }
   int nstage = stages_for(shape, smem);
   if (nstage == 0 && !explicit_shape && shape.warps != 8) {
@@ -423,9 +433,9 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
 // CTAs of the decode step's append encode: one warp per (sequence, KV head)
 // vector, 8 per CTA, keys and values.
 vq_status launch_partial(const vq_layout& L, const vqk::DecodeParams& p, int grid, size_t smem,
-                         void* stream, bool overlap) {
+                         void* stream, bool overlap, int method = vqk::kMethodGather) {
   cudaError_t e = vqk::launch_decode(p, L.k_sub, L.k_bits, L.v_sub, L.v_bits, grid, smem,
-                                     static_cast<cudaStream_t>(stream), overlap);
+                                     static_cast<cudaStream_t>(stream), overlap, method);
   if (e != cudaSuccess) return cuda_fail(e, "decode split kernel");
   return VQ_OK;
 }
@@ -503,6 +513,30 @@ vq_status vq_decode_partial(const vq_layout* layout, int32_t batch, const void* 
                       num_splits, workspace, workspace_bytes, status, p, grid, smem);
   if (st != VQ_OK) return st;
   return launch_partial(*layout, p, grid, smem, stream, false);
+}
+
+vq_status vq_decode_partial_method(const vq_layout* layout, int32_t batch, const void* q,
+                                   const float* lambda, const void* codebook_k,
+                                   const void* codebook_v, const void* k_pool, const void* v_pool,
+                                   int64_t num_pages, const int32_t* page_table,
+                                   int32_t max_pages_per_seq, const int32_t* seq_lens,
+                                   int32_t max_seq_len, float softmax_scale, int32_t num_splits,
+                                   int32_t method, void* workspace, size_t workspace_bytes,
+                                   int32_t* status, void* stream) {
+  vq_status st = check_layout_impl(layout, 1);
+  if (st != VQ_OK) return st;
+  if (method < VQ_METHOD_GATHER || method > VQ_METHOD_BINS)
+    return fail(VQ_ERR_INVALID_ARG, "method %d is not a vq_decode_method", method);
+  if (batch < 0) return fail(VQ_ERR_INVALID_ARG, "batch %d < 0", batch);
+  if (batch == 0) return VQ_OK;
+  vqk::DecodeParams p;
+  int grid = 0;
+  size_t smem = 0;
+  st = prepare_decode(layout, batch, q, lambda, codebook_k, codebook_v, k_pool, v_pool, num_pages,
+                      page_table, max_pages_per_seq, seq_lens, max_seq_len, softmax_scale,
+                      num_splits, workspace, workspace_bytes, status, p, grid, smem, nullptr, method);
+  if (st != VQ_OK) return st;
+  return launch_partial(*layout, p, grid, smem, stream, false, method);
 }
 
 vq_status vq_decode_combine(const vq_layout* layout, int32_t batch, int32_t max_seq_len,

@@ -78,6 +78,12 @@ __device__ __forceinline__ uint32_t row_addr(uint32_t w, uint32_t lw, int i) {
   return __byte_perm(w, lw, 0x5504 | (i << 4));
 }
 
+// The same with 128-byte table rows (one tensor per table, the table-based
+// methods): (code << 7) | lane byte.
+__device__ __forceinline__ uint32_t row7_addr(uint32_t w, uint32_t lw, int i) {
+  return (__byte_perm(w, 0u, 0x4440 | i) << 7) | lw;
+}
+
 // K codes of one token for the lane's 8 (dk = 4) or 16 (dk = 2) sub-vectors.
 template <int DK>
 struct KCodes;
@@ -89,6 +95,12 @@ struct KCodes<4> {
   }
   __device__ __forceinline__ uint32_t off(int i, uint32_t lw) const {
     return row_addr(i < 4 ? w.x : w.y, lw, i & 3);
+  }
+  __device__ __forceinline__ uint32_t off7(int i, uint32_t lw) const {
+    return row7_addr(i < 4 ? w.x : w.y, lw, i & 3);
+  }
+  __device__ __forceinline__ uint32_t code(int i) const {  // code of sub-vector 8c + i
+    return __byte_perm(i < 4 ? w.x : w.y, 0u, 0x4440 | (i & 3));
   }
 };
 template <>
@@ -114,6 +126,7 @@ struct VCodes<4, 8> {
     w = *reinterpret_cast<const uint32_t*>(row + 4 * r);
   }
   __device__ __forceinline__ uint32_t off(int i, uint32_t lw) const { return row_addr(w, lw, i); }
+  __device__ __forceinline__ uint32_t off7(int i, uint32_t lw) const { return row7_addr(w, lw, i); }
 };
 template <>
 struct VCodes<4, 9> {
@@ -401,7 +414,7 @@ __device__ __forceinline__ uint32_t pack_row_word(const int (&idx)[2], int lane)
   return word;
 }
 
-template <int DK, int BK, int DV, int BV, int NG, int NW, bool kAppend>
+template <int DK, int BK, int DV, int BV, int NG, int NW, bool kAppend, int kMethod>
 __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split_kernel(const DecodeParams p) {
   static_assert(BK == 8 || (DK == 8 && BK == 12 && DV == 8 && BV == 12),
                 "K codes are byte-aligned, or the 1.5-bit format (d = 8, 12-bit codes)");
@@ -417,11 +430,16 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   const int G = p.group;
   const int NS = p.nstage;
   static_assert(!kAppend || !kWide, "the 1.5-bit format appends with the encode kernel");
+  static_assert(kMethod == kMethodGather ||
+                    (DK == 4 && BK == 8 && DV == 4 && BV == 8 && NG == 4 && NW == 12 && !kAppend),
+                "the table-based methods are built for d = 4, 8-bit codes, G <= 4");
+  constexpr bool kLut = kMethod == kMethodLut, kBins = kMethod == kMethodBins;
   const DecodeSmem L = decode_smem(BK, BV, G, KROW, VROW, NS, NW, kStageTok,
                                    kAppend ? append_enc_bytes(BK, BV) : 0,
-                                   kAppend ? append_scratch_bytes(NW, DK, DV) : 0);
+                                   kAppend ? append_scratch_bytes(NW, DK, DV) : 0, kMethod);
   float* qt = reinterpret_cast<float*>(smem + L.qt);
-  float* merge = reinterpret_cast<float*>(smem + L.merge);
+  // the LUT method's merge buffer shares the LUT (built again for every unit)
+  float* merge = reinterpret_cast<float*>(smem + (kLut ? L.aux : L.merge));
   float2* mlbuf = reinterpret_cast<float2*>(smem + L.ml);
   int* ulen_c = reinterpret_cast<int*>(smem + L.units);  // unit lengths, consumers' copy
   int* ulen_p = ulen_c + kMaxUnitsPerCta;                  // producers' copy
@@ -691,6 +709,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
     // two rows, so no two lanes share a bank: the replicas of centroid row i
     // reach the lanes by shuffle.
     const uint32_t tab = smem_addr(smem + L.tab);
+    constexpr int kRow = kMethod == kMethodGather ? kTabRow : kTabRow / 2;
     auto fill = [&](const uint2 (&cb)[kNB], int n_i, int rows, int d, uint32_t half) {
 #pragma unroll
       for (int i = 0; i < kNB; ++i) {
@@ -701,7 +720,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
           for (int t = 0; t < 16; ++t) {
             const int src = 2 * t + (lane >> 4);
             const uint32_t x = __shfl_sync(kFull, cb[i].x, src), y = __shfl_sync(kFull, cb[i].y, src);
-            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(tab + (block * 32 + src) * kTabRow + half +
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(tab + (block * 32 + src) * kRow + half +
                                                                   (lane & 15) * 8),
                          "r"(x), "r"(y));
           }
@@ -709,14 +728,27 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
 #pragma unroll 4
           for (int t = 0; t < 32; ++t) {
             const uint32_t x = __shfl_sync(kFull, cb[i].x, t);
-            asm volatile("st.shared.u32 [%0], %1;" ::"r"(tab + (block * 32 + t) * kTabRow + half + lane * 4),
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(tab + (block * 32 + t) * kRow + half + lane * 4),
                          "r"(x));
           }
         }
       }
     };
-    fill(cbk_r, kNK, 1 << BK, DK, 0u);
-    fill(cbv_r, kNV, 1 << BV, DV, 128u);
+    if constexpr (kLut) {         // V only: the scores come from the LUT
+      fill(cbv_r, kNV, 1 << BV, DV, 0u);
+    } else if constexpr (kBins) {  // K only: P.V goes through the bins
+      fill(cbk_r, kNK, 1 << BK, DK, 0u);
+      // the fp32 V codebook for the bins' final product, after the bins
+      float4* cvf = reinterpret_cast<float4*>(smem + L.aux + kLutBytes);
+      if (tid < (1 << BV)) {
+        const __half2 h01 = *reinterpret_cast<const __half2*>(&cbv_r[0].x);
+        const __half2 h23 = *reinterpret_cast<const __half2*>(&cbv_r[0].y);
+        cvf[tid] = make_float4(__low2float(h01), __high2float(h01), __low2float(h23), __high2float(h23));
+      }
+    } else {
+      fill(cbk_r, kNK, 1 << BK, DK, 0u);
+      fill(cbv_r, kNV, 1 << BV, DV, 128u);
+    }
   }
   if (tid < n_units) ulen_c[tid] = len_r[0];  // raw: the append needs the unclamped length
 
@@ -758,13 +790,21 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
         float x[4] = {__low2float(lo) * lam_r.x, __high2float(lo) * lam_r.y,
                       __low2float(hi) * lam_r.z, __high2float(hi) * lam_r.w};
         fwht128_warp(x, lane);
+        if constexpr (kLut) {  // fp32 q~ [head][128] for the LUT
+          reinterpret_cast<float4*>(qt + warp * kHeadDim)[lane] =
+              make_float4(x[0] * p.qscale, x[1] * p.qscale, x[2] * p.qscale, x[3] * p.qscale);
+        }
         split_half2(x[0] * p.qscale, x[1] * p.qscale, h01, l01);
         split_half2(x[2] * p.qscale, x[3] * p.qscale, h23, l23);
         load_q(k + 1);  // prefetch the next unit's query
+      } else if constexpr (kLut) {
+        reinterpret_cast<float4*>(qt + warp * kHeadDim)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      uint32_t* qf = reinterpret_cast<uint32_t*>(qt) + (warp * 2 * 4 + (lane >> 3)) * 16 + 2 * (lane & 7);
-      *reinterpret_cast<uint2*>(qf) = make_uint2(h01, h23);
-      *reinterpret_cast<uint2*>(qf + 4 * 16) = make_uint2(l01, l23);
+      if constexpr (!kLut) {
+        uint32_t* qf = reinterpret_cast<uint32_t*>(qt) + (warp * 2 * 4 + (lane >> 3)) * 16 + 2 * (lane & 7);
+        *reinterpret_cast<uint2*>(qf) = make_uint2(h01, h23);
+        *reinterpret_cast<uint2*>(qf + 4 * 16) = make_uint2(l01, l23);
+      }
     }
   };
   // Fused append: encodes the new token of unit u's (sequence, KV head)
@@ -857,7 +897,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   // the lane's byte inside a table row: its replica of the K (bytes 0..127)
   // or V (bytes 128..255) centroid, one bank pair (8-byte) or bank (4-byte) per lane
   const uint32_t lwk = kWide ? 0u : DK == 4 ? (lane & 15) * 8 : lane * 4;
-  const uint32_t lwv = kWide ? 65536u : 128 + (DV == 4 ? (lane & 15) * 8 : lane * 4);
+  const uint32_t lwv = kWide ? 65536u : (kLut ? 0u : 128u) + (DV == 4 ? (lane & 15) * 8 : lane * 4);
   uint32_t qa[8][2];  // score B operands: NG == 4: columns (2g: hi, 2g+1: lo); NG == 8: hi
   uint32_t qb[8][2];  // NG == 8: lo
   float O[8][4];      // output accumulators (NG == 4 uses O[0..3])
@@ -882,6 +922,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   // lane-constant byte offsets of the lane's code rows inside a stage
   const int koff0 = (warp * kChunk + r) * KROW, koff1 = koff0 + 8 * KROW;
   const int voff = kStageTok * KROW + warp * kChunk * VROW;
+  const int voff0 = voff;  // the warp's V rows (bins method: whole rows of tokens r and r+8)
   auto load_codes = [&](const uint8_t* st) {
     kc[0].load(st + koff0, c);
     kc[1].load(st + koff1, c);
@@ -906,14 +947,23 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   //    sub-vectors 8r + 2q, 8r + 2q + 1 (dv = 2); lane (r, c) accumulates dims
   //    16r + 4q .. 16r + 4q + 3 of head c.
   //  G > 4: reduction over 16 tokens, A = V^T built with PRMT (pairs of tokens).
+  // gather offsets: 256-byte table rows, or 128-byte rows for the table-based methods
+  auto vgoff = [&](const VCodes<DV, BV>& v, int i) -> uint32_t {
+    if constexpr (kLut) return v.off7(i, lwv);
+    else return v.off(i, lwv);
+  };
+  auto kgoff = [&](const KCodes<DK>& kcd, int i) -> uint32_t {
+    if constexpr (kBins) return kcd.off7(i, lwk);
+    else return kcd.off(i, lwk);
+  };
   auto pv_step = [&](int q) {
     if constexpr (NG == 4) {
 #pragma unroll
       for (int ks = 0; ks < 2; ++ks) {  // tokens 8ks + c and 8ks + c + 4
         uint32_t a0, a1, a2, a3;
         if constexpr (DV >= 4) {
-          const uint2 w0 = tab64(pvc[2 * ks].off(q, lwv));
-          const uint2 w1 = tab64(pvc[2 * ks + 1].off(q, lwv));
+          const uint2 w0 = tab64(vgoff(pvc[2 * ks], q));
+          const uint2 w1 = tab64(vgoff(pvc[2 * ks + 1], q));
           a0 = w0.x; a1 = w0.y; a2 = w1.x; a3 = w1.y;
         } else {
           a0 = tab32(pvc[2 * ks].off(2 * q, lwv));
@@ -957,8 +1007,8 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       if (with_qk) {
         uint32_t a0, a1, a2, a3;
         if constexpr (DK >= 4) {
-          const uint2 g0 = tab64(kc[0].off(kk, lwk));
-          const uint2 g1 = tab64(kc[1].off(kk, lwk));
+          const uint2 g0 = tab64(kgoff(kc[0], kk));
+          const uint2 g1 = tab64(kgoff(kc[1], kk));
           a0 = g0.x; a1 = g1.x; a2 = g0.y; a3 = g1.y;
         } else {
           a0 = tab32(kc[0].off(2 * kk, lwk));
@@ -969,10 +1019,138 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
         mma16816(acc, a0, a1, a2, a3, qa[kk][0], qa[kk][1]);
         if constexpr (NG == 8) mma16816(acc2, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
       }
-      if ((kk & 1) == 0) pv_step(kk >> 1);
+      if constexpr (!kBins) {
+        if ((kk & 1) == 0) pv_step(kk >> 1);
+      }
     }
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) sc[jj] = NG == 8 ? acc[jj] + acc2[jj] : acc[jj];
+  };
+
+  // LUT method: scores of the warp's chunk from the per-query table
+  // LUT[i][j][g] = q~_g[4i .. 4i+3] . C_k[j] (fp32, [subspace][code][head]):
+  // lane (r, c) sums subspaces 8c .. 8c+7 of tokens r and r+8 for every head,
+  // the four lanes of a row add their sums by shuffle, and the lane keeps head
+  // c, the score layout the softmax takes (hi part = score, lo part = 0).  The
+  // previous chunk's P.V runs in the same block, as in `fused`.
+  auto fused_lut = [&](float (&sc)[4], bool with_qk) {
+   if constexpr (kLut) {
+    const float4* lut = reinterpret_cast<const float4*>(smem + L.aux) + 8 * c * 256;
+    float a[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      if (with_qk) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const float4 e = lut[kk * 256 + kc[t].code(kk)];
+          a[t][0] += e.x;
+          a[t][1] += e.y;
+          a[t][2] += e.z;
+          a[t][3] += e.w;
+        }
+      }
+      if ((kk & 1) == 0) pv_step(kk >> 1);
+    }
+    if (with_qk) {
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          a[t][g] += __shfl_xor_sync(kFull, a[t][g], 1);
+          a[t][g] += __shfl_xor_sync(kFull, a[t][g], 2);
+        }
+      sc[0] = c == 0 ? a[0][0] : c == 1 ? a[0][1] : c == 2 ? a[0][2] : a[0][3];
+      sc[2] = c == 0 ? a[1][0] : c == 1 ? a[1][1] : c == 2 ? a[1][2] : a[1][3];
+      sc[1] = sc[3] = 0.f;
+    }
+   }
+  };
+
+  // LUT method: the table of the unit's q~ (built after q~ is visible).
+  auto build_lut = [&]() {
+    if constexpr (kLut) {
+      float4* lut = reinterpret_cast<float4*>(smem + L.aux);
+      const float4* q4 = reinterpret_cast<const float4*>(qt);  // fp32 q~ [head][128]
+      for (int e = tid; e < 32 * 256; e += kConsumerThreads) {
+        const int i = e >> 8, j = e & 255;
+        const uint2 cw = __ldg(reinterpret_cast<const uint2*>(p.cb_k) + j);
+        const __half2 c01 = *reinterpret_cast<const __half2*>(&cw.x), c23 = *reinterpret_cast<const __half2*>(&cw.y);
+        const float c0 = __low2float(c01), c1 = __high2float(c01), c2 = __low2float(c23), c3 = __high2float(c23);
+        float v[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const float4 qg = q4[g * (kHeadDim / 4) + i];
+          v[g] = fmaf(qg.w, c3, fmaf(qg.z, c2, fmaf(qg.y, c1, qg.x * c0)));
+        }
+        lut[e] = make_float4(v[0], v[1], v[2], v[3]);
+      }
+    }
+  };
+
+  // Bins method: p of every (token, subspace) is added into bins[i][code][head]
+  // (fp32, shared by the consumer warps); at the end of the unit o_g[4i + e] =
+  // sum_j bins[i][j][g] C_v[j][e].  The warps share one reference maximum per
+  // head, so each stage first agrees on the stage's maximum (a consumer
+  // barrier) and, when it grew by more than kLazyLog2, rescales the bins.
+  float mref = -INFINITY;  // bins method: this lane's head (c) reference
+  auto bins_update = [&](const float (&sc)[4], const uint4 (&vr)[2][2], int tok0, int lim, bool live,
+                         int par) {
+    if constexpr (kBins) {
+      float* bins = reinterpret_cast<float*>(smem + L.aux);
+      float* smax = reinterpret_cast<float*>(mlbuf);  // [2][NW][4]: the stage maxima per warp and head
+      float s0 = sc[0] + sc[1], s1 = sc[2] + sc[3];   // head c, tokens r and r+8
+      if (!live || tok0 + kChunk > lim) {
+        const int lim_n = live ? lim : 0;
+        s0 = tok0 + r < lim_n ? s0 : -INFINITY;
+        s1 = tok0 + r + 8 < lim_n ? s1 : -INFINITY;
+      }
+      float mx = fmaxf(s0, s1);
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+      if (r == 0) smax[(par * NW + warp) * 4 + c] = mx;
+      consumer_sync<NW>();
+      float M = mref;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, smax[(par * NW + w) * 4 + c]);
+      // every warp reads the same maxima, so the decision is the same in all of them
+      if (__any_sync(kFull, M > mref + kLazyLog2)) {
+        const bool grows = M > mref + kLazyLog2;
+        const float alpha = !grows ? 1.f : mref == -INFINITY ? 0.f : fast_exp2(mref - M);
+        float al[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) al[g] = __shfl_sync(kFull, alpha, g);  // lane g holds head g
+        float4* b4 = reinterpret_cast<float4*>(bins);
+        for (int e = tid; e < 32 * 256; e += kConsumerThreads) {
+          float4 b = b4[e];
+          b.x *= al[0];
+          b.y *= al[1];
+          b.z *= al[2];
+          b.w *= al[3];
+          b4[e] = b;
+        }
+        l_run[0] *= alpha;
+        if (grows) mref = M;
+        consumer_sync<NW>();  // the bins are at the new reference before any warp adds to them
+      }
+      const float mr = mref == -INFINITY ? 0.f : mref;
+      const float p0 = fast_exp2(s0 - mr), p1 = fast_exp2(s1 - mr);
+      l_run[0] += p0 + p1;
+      const uint32_t base = smem_addr(bins) + 4u * c;  // + ((i * 256 + code) * 4) * 4
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const float pt = t ? p1 : p0;
+        if (pt != 0.f) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const uint32_t w = (i < 16) ? (i < 8 ? (i < 4 ? vr[t][0].x : vr[t][0].y) : (i < 12 ? vr[t][0].z : vr[t][0].w))
+                                        : (i < 24 ? (i < 20 ? vr[t][1].x : vr[t][1].y) : (i < 28 ? vr[t][1].z : vr[t][1].w));
+            const uint32_t code = __byte_perm(w, 0u, 0x4440 | (i & 3));
+            asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(base + i * 4096u + (code << 4)), "f"(pt) : "memory");
+          }
+        }
+      }
+    }
   };
 
   // Online softmax (log2 domain) over the current chunk: updates m and l,
@@ -1075,7 +1253,10 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
     // B operands of the score mma: k-step kk, rows {2c, 2c+1, 2c+8, 2c+9} hold
     // dims 32c + 4kk + {0, 1, 2, 3}; column = r (G <= 4: head r / 2, hi part
     // for even r, lo for odd r; G > 4: head r, hi in qa and lo in qb).
-    {
+    if constexpr (kLut) {
+      build_lut();
+      consumer_sync<NW>();  // the unit's LUT is complete
+    } else {
       const uint4* qf = reinterpret_cast<const uint4*>(qt);
       if constexpr (NG == 4) {
         const int blk = ((r >> 1) * 2 + (r & 1)) * 4 + c;
@@ -1112,6 +1293,12 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       m_run[gi] = -INFINITY;
       l_run[gi] = 0.f;
     }
+    if constexpr (kBins) {  // empty bins at no reference
+      float4* b4 = reinterpret_cast<float4*>(smem + L.aux);
+      for (int e = tid; e < 32 * 256; e += kConsumerThreads) b4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+      mref = -INFINITY;
+      consumer_sync<NW>();
+    }
     if (k == 0) pdl_wait();  // partials are written only after the previous kernel completes
     pb[0][0] = pb[0][1] = pb[1][0] = pb[1][1] = 0u;  // nothing pending yet
 #pragma unroll
@@ -1130,22 +1317,46 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       const int4 m = meta[slot];
       const int tok0 = m.x + warp * kChunk;      // first token of the warp's chunk
       const bool live = ok && ((static_cast<uint32_t>(m.z) >> warp) & 1u) && tok0 < m.y;
-      load_codes(stages + slot * kStageBytes);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty + slot);  // codes are in registers: the slot may be refilled
-      if (++slot == NS) {
-        slot = 0;
-        phase ^= 1u;
-      }
-      float sc[4];
-      fused(sc, true);                           // scores now, P.V of the previous stage
-      softmax(sc, tok0, m.y, live);              // tokens past the end and invalid pages: p = 0
+      if constexpr (kBins) {
+        const uint8_t* st = stages + slot * kStageBytes;
+        kc[0].load(st + koff0, c);
+        kc[1].load(st + koff1, c);
+        uint4 vr[2][2];  // V rows of tokens r and r+8 (32 codes each)
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) pvc[jj] = vc[jj];
+        for (int t = 0; t < 2; ++t) {
+          const uint4* row = reinterpret_cast<const uint4*>(st + voff0 + (r + 8 * t) * VROW);
+          vr[t][0] = row[0];
+          vr[t][1] = row[1];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty + slot);
+        if (++slot == NS) {
+          slot = 0;
+          phase ^= 1u;
+        }
+        float sc[4];
+        fused(sc, true);                         // scores only
+        bins_update(sc, vr, tok0, m.y, live, j & 1);
+      } else {
+        load_codes(stages + slot * kStageBytes);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty + slot);  // codes are in registers: the slot may be refilled
+        if (++slot == NS) {
+          slot = 0;
+          phase ^= 1u;
+        }
+        float sc[4];
+        if constexpr (kLut) fused_lut(sc, true);
+        else fused(sc, true);                      // scores now, P.V of the previous stage
+        softmax(sc, tok0, m.y, live);              // tokens past the end and invalid pages: p = 0
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) pvc[jj] = vc[jj];
+      }
     }
-    {  // P.V of the unit's last stage
+    if constexpr (!kBins) {  // P.V of the unit's last stage
       float sc[4];
-      fused(sc, false);
+      if constexpr (kLut) fused_lut(sc, false);
+      else fused(sc, false);
     }
 
     // ---- merge the consumer warps of this unit, write the split partial ------
@@ -1155,6 +1366,55 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       l_run[gi] += __shfl_xor_sync(kFull, l_run[gi], 8);
       l_run[gi] += __shfl_xor_sync(kFull, l_run[gi], 16);
     }
+    if constexpr (kBins) {
+      // every stage's additions are in; the stage-maximum buffer holds the sums next
+      consumer_sync<NW>();
+      float* lsum = reinterpret_cast<float*>(mlbuf);  // [NW][4]
+      if (r == 0) lsum[warp * 4 + c] = l_run[0];
+      consumer_sync<NW>();
+      // o_g[4i + e] = sum_j bins[i][j][g] C_v[j][e]: warp w takes subspaces w, w + NW, ...;
+      // lane l the codes l, l + 32, ..., then a shuffle reduction
+      const float4* b4 = reinterpret_cast<const float4*>(smem + L.aux);
+      const float4* cvf = reinterpret_cast<const float4*>(smem + L.aux + kLutBytes);
+      for (int i = warp; i < 32; i += NW) {
+        float acc[4][4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[g][e] = 0.f;
+#pragma unroll
+        for (int m8 = 0; m8 < 8; ++m8) {
+          const int j = lane + 32 * m8;
+          const float4 b = b4[i * 256 + j], cv = cvf[j];
+          const float bg[4] = {b.x, b.y, b.z, b.w}, ce[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[g][e] = fmaf(bg[g], ce[e], acc[g][e]);
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+#pragma unroll
+            for (int sh = 16; sh >= 1; sh >>= 1) acc[g][e] += __shfl_xor_sync(kFull, acc[g][e], sh);
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          if (lane == g && g < G) {
+            const long long row = (static_cast<long long>(u.b) * p.hq + u.kvh * G + g) * p.splits + u.s;
+            reinterpret_cast<float4*>(p.ws_o + row * kHeadDim)[i] =
+                make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+          }
+      }
+      if (warp == 0 && lane < G) {  // lane g (row 0, column g) holds head g's reference
+        float l = 0.f;
+        for (int w = 0; w < NW; ++w) l += lsum[w * 4 + lane];
+        const long long row = (static_cast<long long>(u.b) * p.hq + u.kvh * G + lane) * p.splits + u.s;
+        p.ws_ml[row] = make_float2(mref, mref == -INFINITY ? 0.f : l);
+      }
+      continue;  // the next unit starts with a consumer barrier
+    }
+    if constexpr (kLut) consumer_sync<NW>();  // the merge buffer is the LUT: every warp is done with it
     if constexpr (NG == 4) {
       if (c < G) {
         float4* mo = reinterpret_cast<float4*>(merge + (warp * G + c) * kHeadDim + 16 * r);
@@ -1205,10 +1465,10 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   __syncthreads();  // matches the producers' final barrier
 }
 
-template <int DK, int BK, int DV, int BV, int NG, int NW, bool kAppend>
+template <int DK, int BK, int DV, int BV, int NG, int NW, bool kAppend, int kMethod = kMethodGather>
 cudaError_t launch_split(const DecodeParams& p, int grid, size_t smem, cudaStream_t stream,
                          bool overlap) {
-  auto kern = vq_decode_split_kernel<DK, BK, DV, BV, NG, NW, kAppend>;
+  auto kern = vq_decode_split_kernel<DK, BK, DV, BV, NG, NW, kAppend, kMethod>;
   static SmemOptIn opt_in;
   cudaError_t e = ensure_smem(kern, smem, opt_in);
   if (e != cudaSuccess) return e;
@@ -1218,8 +1478,17 @@ cudaError_t launch_split(const DecodeParams& p, int grid, size_t smem, cudaStrea
 
 template <int DK, int BK, int DV, int BV>
 cudaError_t launch_formats(const DecodeParams& p, int grid, size_t smem, cudaStream_t stream,
-                           bool ov) {
+                           bool ov, int method) {
   const bool wide = p.group > 4;
+  if (method != kMethodGather) {  // the table-based methods: d = 4, 8-bit codes, G <= 4, 12 warps
+    if constexpr (DK == 4 && BK == 8 && DV == 4 && BV == 8) {
+      if (!wide && p.warps == 12 && !p.append) {
+        if (method == kMethodLut) return launch_split<4, 8, 4, 8, 4, 12, false, kMethodLut>(p, grid, smem, stream, ov);
+        if (method == kMethodBins) return launch_split<4, 8, 4, 8, 4, 12, false, kMethodBins>(p, grid, smem, stream, ov);
+      }
+    }
+    return cudaErrorInvalidValue;
+  }
   if (p.append) {  // the decode step with the append inside: the default shapes only
     if constexpr (BK <= 9 && BV <= 9) {
       if (p.warps == 12 && !wide) return launch_split<DK, BK, DV, BV, 4, 12, true>(p, grid, smem, stream, ov);
@@ -1241,9 +1510,10 @@ cudaError_t launch_formats(const DecodeParams& p, int grid, size_t smem, cudaStr
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, int k_sub, int k_bits, int v_sub, int v_bits,
-                          int grid, size_t smem, cudaStream_t stream, bool overlap) {
+                          int grid, size_t smem, cudaStream_t stream, bool overlap, int method) {
 #define VQ_CASE(DK, BK, DV, BV) \
-  if (k_sub == DK && k_bits == BK && v_sub == DV && v_bits == BV) return launch_formats<DK, BK, DV, BV>(p, grid, smem, stream, overlap);
+  if (k_sub == DK && k_bits == BK && v_sub == DV && v_bits == BV) \
+    return launch_formats<DK, BK, DV, BV>(p, grid, smem, stream, overlap, method);
   VQ_CASE(2, 8, 4, 8)
   VQ_CASE(4, 8, 4, 8)
   VQ_CASE(2, 8, 4, 9)

@@ -127,8 +127,19 @@ struct DecodeShape {
 // centroids of 8 elements) has no replicas: 32 bytes per centroid index, laid
 // out half-major ([tensor][half][code] x 8 bytes).
 struct DecodeSmem {
-  int tab, qt, merge, ml, units, meta, bar, flag, enc, stage, total;
+  int tab, qt, merge, ml, units, meta, bar, flag, enc, aux, stage, total;
 };
+
+// Score and P.V methods of the split kernel (the pages' alternatives):
+//   kMethodGather: scores and P.V from centroid gathers on the tensor cores;
+//   kMethodLut:    scores from a per-query, per-subspace lookup table
+//                  q~_i . C_k[j] summed over the K codes, P.V by gather;
+//   kMethodBins:   scores by gather, P.V by accumulating p into per-code bins,
+//                  multiplied by the V codebook at the end of each unit.
+// The table-based methods exist for d = 4, 8-bit K and V codes, G <= 4.
+enum DecodeMethod : int { kMethodGather = 0, kMethodLut = 1, kMethodBins = 2 };
+
+constexpr int kLutBytes = 32 * 256 * 4 * 4;  // [subspace][code][head] fp32: the LUT or the bins
 
 constexpr int kTabRow = 256;      // bytes per codebook table row (replicated centroids)
 constexpr int kTabRowWide = 32;   // 1.5-bit format (12-bit codes): K and V centroid, no replicas
@@ -150,22 +161,28 @@ __host__ __device__ inline int append_scratch_bytes(int warps, int k_sub, int v_
 }
 
 // append_enc / append_scratch: the fused append's table and scratch bytes (0: no append)
+// method: a DecodeMethod; the table-based ones keep only the gathered
+// tensor's centroids in the replicated table (128-byte rows), the LUT or the
+// bins in `aux` (the LUT method's merge buffer shares it), and the bins
+// method's fp32 V codebook after them.
 __host__ __device__ inline DecodeSmem decode_smem(int k_bits, int v_bits, int group, int k_row,
                                                   int v_row, int nstage, int warps, int stage_tok,
-                                                  int append_enc = 0, int append_scratch = 0) {
+                                                  int append_enc = 0, int append_scratch = 0,
+                                                  int method = 0) {
   DecodeSmem s;
   int o = 0;
   const int rows = 1 << (k_bits > v_bits ? k_bits : v_bits);
-  s.tab = o; o = align128(o + rows * (k_bits == 12 ? kTabRowWide : kTabRow));
+  s.tab = o; o = align128(o + rows * (k_bits == 12 ? kTabRowWide : method ? kTabRow / 2 : kTabRow));
   s.qt = o; o = align128(o + (group > 4 ? 8 : 4) * 128 * 4);  // q~ operand table, 4 or 8 heads
-  const int merge = warps * group * 128 * 4;
+  const int merge = method ? 0 : warps * group * 128 * 4;
   s.merge = o; o = align128(o + (merge > append_scratch ? merge : append_scratch));
-  s.ml = o; o = align128(o + warps * group * 8);
+  s.ml = o; o = align128(o + warps * (group > 4 ? 8 : 4) * 8);
   s.units = o; o = align128(o + 2 * kMaxUnitsPerCta * 4);  // consumer and producer copies
   s.meta = o; o = align128(o + nstage * 16);
   s.bar = o; o = align128(o + (nstage * 2 + 1) * 8);  // full and empty per slot, then the append's
   s.flag = o; o = align128(o + 16);
   s.enc = o; o = align128(o + append_enc);
+  s.aux = o; o = align128(o + (method ? kLutBytes : 0) + (method == 2 ? (1 << v_bits) * 4 * 4 : 0));
   s.stage = o; o = align128(o + nstage * stage_tok * (k_row + v_row));
   s.total = o;
   return s;
@@ -231,7 +248,8 @@ size_t encode_smem_bytes(int sub, int bits);
 
 // Returns cudaErrorInvalidValue when no kernel is compiled for the formats.
 cudaError_t launch_decode(const DecodeParams& p, int k_sub, int k_bits, int v_sub, int v_bits,
-                          int grid, size_t smem, cudaStream_t stream, bool overlap);
+                          int grid, size_t smem, cudaStream_t stream, bool overlap,
+                          int method = kMethodGather);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool overlap);
 cudaError_t launch_dequant(const DequantParams& p, int grid_x, cudaStream_t stream);
 cudaError_t launch_residual(const ResidualParams& p, int grid, cudaStream_t stream, bool overlap);

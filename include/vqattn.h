@@ -248,6 +248,44 @@ vq_status vq_decode_combine(const vq_layout* layout, int32_t batch, int32_t max_
                             void* out, void* stream);
 
 /*
+ * Score and P.V methods of the split attention kernel.  The pages name two
+ * ways for each half of the attention over codes (VecInfer, 内核实现细节 -
+ * 融合内核, Algorithm 1: a lookup table of query x K-codebook products summed
+ * over the codes; CommVQ, 降低计算复杂度: Softmax(A) S_V C_V, i.e. P.V by
+ * accumulating p into per-code bins and multiplying by the V codebook once):
+ *   VQ_METHOD_GATHER  scores and P.V from in-register centroid gathers on the
+ *                     tensor cores (what every other call uses);
+ *   VQ_METHOD_LUT     scores from the table LUT[i][j] = q~_i . C_k[j] (fp32,
+ *                     built per work unit), P.V by gather;
+ *   VQ_METHOD_BINS    scores by gather, P.V through fp32 bins[i][j] += p,
+ *                     o_i = sum_j bins[i][j] C_v[j] at the end of each unit.
+ */
+typedef enum vq_decode_method {
+  VQ_METHOD_GATHER = 0,
+  VQ_METHOD_LUT = 1,
+  VQ_METHOD_BINS = 2
+} vq_decode_method;
+
+/*
+ * vq_decode_partial with an explicit method (above), for measuring the
+ * methods against each other; vq_decode_combine then merges the partials as
+ * usual.  The results agree with every method's within fp32 rounding (the
+ * bins method adds in an order that varies from run to run).  The table-based
+ * methods are built for k_sub = v_sub = 4 with 8-bit codes and
+ * num_q_heads / num_kv_heads <= 4; other layouts return VQ_ERR_UNSUPPORTED.
+ * The bins method keeps one reference maximum per head for the whole work
+ * unit, agreed between the warps at every pipeline stage.
+ */
+vq_status vq_decode_partial_method(const vq_layout* layout, int32_t batch, const void* q,
+                                   const float* lambda, const void* codebook_k,
+                                   const void* codebook_v, const void* k_pool, const void* v_pool,
+                                   int64_t num_pages, const int32_t* page_table,
+                                   int32_t max_pages_per_seq, const int32_t* seq_lens,
+                                   int32_t max_seq_len, float softmax_scale, int32_t num_splits,
+                                   int32_t method, void* workspace, size_t workspace_bytes,
+                                   int32_t* status, void* stream);
+
+/*
  * One decode step: append each sequence's new token to the cache, then decode
  * attention over the cache with the new token included (VecInfer, section
  * 方法细节 "注意力机制中的向量量化KV缓存": during decoding the new key and value
