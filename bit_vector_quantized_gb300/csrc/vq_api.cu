@@ -302,7 +302,7 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
                          float softmax_scale, int32_t num_splits, const void* workspace,
                          size_t workspace_bytes, int32_t* status, vqk::DecodeParams& p,
                          int& grid, size_t& smem, bool* append = nullptr,
-                         int method = vqk::kMethodGather) {
+                         int method = vqk::kMethodGather, bool residual = false) {
   const vq_layout& L = *layout;
   const void* ptrs[] = {q, lambda, codebook_k, codebook_v, k_pool, v_pool, page_table, seq_lens, workspace};
   const char* names[] = {"q", "lambda", "codebook_k", "codebook_v", "k_pool", "v_pool",
@@ -377,7 +377,7 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
       bytes = vqk::decode_smem(L.k_bits, L.v_bits, p.group, p.k_row, p.v_row, ns, sh.warps,
                                sh.stage_tok(), with_append ? vqk::append_enc_bytes(L.k_bits, L.v_bits) : 0,
                                with_append ? vqk::append_scratch_bytes(sh.warps, L.k_sub, L.v_sub) : 0,
-                               method)
+                               method, residual ? 1 : 0)
                   .total;
       if (optin <= 0 || bytes <= static_cast<size_t>(optin)) return ns;
     }
@@ -813,33 +813,26 @@ vq_status vq_decode_attention_residual(const vq_layout* layout, int32_t batch, c
   size_t smem = 0;
   st = prepare_decode(layout, batch, q, lambda, codebook_k, codebook_v, k_pool, v_pool, num_pages,
                       page_table, max_pages_per_seq, seq_lens, max_seq_len, softmax_scale,
-                      num_splits, workspace, workspace_bytes, status, p, grid, smem);
+                      num_splits, workspace, workspace_bytes, status, p, grid, smem, nullptr,
+                      vqk::kMethodGather, true);
   if (st != VQ_OK) return st;
   const ResLayout r = res_layout(L, batch, p.splits);
   if (workspace_bytes < r.total)
     return fail(VQ_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, r.total);
 
-  // 1. the residual window's partial, 2. split attention over the codes, 3. merge
-  vqk::ResidualParams rp{};
+  // 1. split attention over the codes with the residual window's partial
+  // computed inside (by the unit of each pair's last split), 2. merge
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
-  rp.q = q;
-  rp.k_res = k_res;
-  rp.v_res = v_res;
-  rp.res_lens = res_lens;
-  rp.res_o = reinterpret_cast<float*>(wsb + r.o_off);
-  rp.res_ml = reinterpret_cast<float2*>(wsb + r.ml_off);
+  p.residual = 1;
+  p.k_res = k_res;
+  p.v_res = v_res;
+  p.res_lens = res_lens;
+  p.res_capacity = res_capacity;
+  p.res_o = reinterpret_cast<float*>(wsb + r.o_off);
+  p.res_ml = reinterpret_cast<float2*>(wsb + r.ml_off);
   const float scale = softmax_scale == 0.f ? 1.f / std::sqrt(static_cast<float>(L.head_dim)) : softmax_scale;
-  rp.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  rp.hq = L.num_q_heads;
-  rp.hkv = L.num_kv_heads;
-  rp.group = L.num_q_heads / L.num_kv_heads;
-  rp.capacity = res_capacity;
-  const long long rgrid = static_cast<long long>(batch) * L.num_kv_heads;
-  if (rgrid > 0x7fffffffLL) return fail(VQ_ERR_INVALID_ARG, "batch %d too large", batch);
-  cudaError_t e = vqk::launch_residual(rp, static_cast<int>(rgrid), static_cast<cudaStream_t>(stream),
-                                       false);
-  if (e != cudaSuccess) return cuda_fail(e, "residual attention kernel");
-  st = launch_partial(L, p, grid, smem, stream, true);
+  p.res_scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  st = launch_partial(L, p, grid, smem, stream, false);
   if (st != VQ_OK) return st;
   return combine_impl(layout, batch, max_seq_len, p.splits, workspace, workspace_bytes, out, stream,
                       true, true);

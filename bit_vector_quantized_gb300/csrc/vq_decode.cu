@@ -414,7 +414,7 @@ __device__ __forceinline__ uint32_t pack_row_word(const int (&idx)[2], int lane)
   return word;
 }
 
-template <int DK, int BK, int DV, int BV, int NG, int NW, bool kAppend, int kMethod>
+template <int DK, int BK, int DV, int BV, int NG, int NW, bool kAppend, int kMethod, bool kResidual>
 __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split_kernel(const DecodeParams p) {
   static_assert(BK == 8 || (DK == 8 && BK == 12 && DV == 8 && BV == 12),
                 "K codes are byte-aligned, or the 1.5-bit format (d = 8, 12-bit codes)");
@@ -434,9 +434,11 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
                     (DK == 4 && BK == 8 && DV == 4 && BV == 8 && NG == 4 && NW == 12 && !kAppend),
                 "the table-based methods are built for d = 4, 8-bit codes, G <= 4");
   constexpr bool kLut = kMethod == kMethodLut, kBins = kMethod == kMethodBins;
+  static_assert(!kResidual || (kMethod == kMethodGather && !kAppend), "the residual window runs alone");
   const DecodeSmem L = decode_smem(BK, BV, G, KROW, VROW, NS, NW, kStageTok,
                                    kAppend ? append_enc_bytes(BK, BV) : 0,
-                                   kAppend ? append_scratch_bytes(NW, DK, DV) : 0, kMethod);
+                                   kAppend ? append_scratch_bytes(NW, DK, DV) : 0, kMethod,
+                                   kResidual ? 1 : 0);
   float* qt = reinterpret_cast<float*>(smem + L.qt);
   // the LUT method's merge buffer shares the LUT (built again for every unit)
   float* merge = reinterpret_cast<float*>(smem + (kLut ? L.aux : L.merge));
@@ -1241,11 +1243,126 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
     }
   };
 
+  // Full-precision residual window (VecInfer, 实验结果 / 实验设置: the most
+  // recent tokens stay unquantized): the unit of a (sequence, KV head)'s last
+  // split turns the window's R tokens into one more partial in the log2
+  // domain of the split partials, s = q . k * scale * log2(e) with the raw
+  // query and keys.  Warp w takes tokens w, w + NW, ... (kRB of its rows in
+  // flight at a time) with an online softmax
+  // per head (lane l holds elements 4l .. 4l+3 of the key, the value and the
+  // sum of p v); the warps' partials merge through the merge buffer.
+  auto residual_partial = [&](const UnitStages& u) {
+    if constexpr (kResidual) {
+      int R = __ldg(p.res_lens + u.b);
+      R = R < 0 ? 0 : (R > p.res_capacity ? p.res_capacity : R);
+      const long long head = static_cast<long long>(u.b) * p.hkv + u.kvh;
+      const uint2* kr = reinterpret_cast<const uint2*>(static_cast<const __half*>(p.k_res) +
+                                                       head * p.res_capacity * kHeadDim);
+      const uint2* vr = reinterpret_cast<const uint2*>(static_cast<const __half*>(p.v_res) +
+                                                       head * p.res_capacity * kHeadDim);
+      auto unpack = [](uint2 w, float (&f)[4]) {
+        const __half2 lo = *reinterpret_cast<const __half2*>(&w.x), hi = *reinterpret_cast<const __half2*>(&w.y);
+        f[0] = __low2float(lo);
+        f[1] = __high2float(lo);
+        f[2] = __low2float(hi);
+        f[3] = __high2float(hi);
+      };
+      float qv[NG][4], acc[NG][4], mr[NG], lr[NG];
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        mr[g] = -INFINITY;
+        lr[g] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) qv[g][e] = acc[g][e] = 0.f;
+        if (g < G) {
+          float f[4];
+          unpack(__ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.q) +
+                                                     (static_cast<long long>(u.b) * p.hq + u.kvh * G + g) * kHeadDim) +
+                       lane),
+                 f);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) qv[g][e] = f[e] * p.res_scale_log2;
+        }
+      }
+      constexpr int kRB = 4;  // tokens per warp whose rows are in flight together
+      for (int t0 = warp; t0 < R; t0 += kRB * NW) {
+        uint2 kk[kRB], vv[kRB];
+#pragma unroll
+        for (int i = 0; i < kRB; ++i) {
+          const int t = t0 + i * NW;
+          kk[i] = t < R ? __ldg(kr + static_cast<long long>(t) * (kHeadDim / 4) + lane) : make_uint2(0u, 0u);
+          vv[i] = t < R ? __ldg(vr + static_cast<long long>(t) * (kHeadDim / 4) + lane) : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < kRB; ++i) {
+          if (t0 + i * NW >= R) break;  // uniform over the warp
+          float kf[4], vf[4];
+          unpack(kk[i], kf);
+          unpack(vv[i], vf);
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            if (g >= G) break;
+            float a = qv[g][0] * kf[0];
+            a = fmaf(qv[g][1], kf[1], a);
+            a = fmaf(qv[g][2], kf[2], a);
+            a = fmaf(qv[g][3], kf[3], a);
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) a += __shfl_xor_sync(kFull, a, o);
+            const float mn = fmaxf(mr[g], a);
+            const float al = fast_exp2(mr[g] - mn);  // 0 from -inf
+            const float pr = fast_exp2(a - mn);
+            lr[g] = fmaf(lr[g], al, pr);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[g][e] = fmaf(acc[g][e], al, pr * vf[e]);
+            mr[g] = mn;
+          }
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        if (g >= G) break;
+        reinterpret_cast<float4*>(merge + (warp * G + g) * kHeadDim)[lane] =
+            make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+        if (lane == 0) mlbuf[warp * G + g] = make_float2(mr[g], lr[g]);
+      }
+      consumer_sync<NW>();
+      for (int i = tid; i < G * (kHeadDim / 4); i += kConsumerThreads) {
+        const int g = i / (kHeadDim / 4), d4 = i % (kHeadDim / 4);
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, mlbuf[w * G + g].x);
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        float l = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < NW; ++w) {
+            const float2 ml = mlbuf[w * G + g];
+            const float f = fast_exp2(ml.x - M);
+            const float4 v = reinterpret_cast<const float4*>(merge + (w * G + g) * kHeadDim)[d4];
+            o.x = fmaf(f, v.x, o.x);
+            o.y = fmaf(f, v.y, o.y);
+            o.z = fmaf(f, v.z, o.z);
+            o.w = fmaf(f, v.w, o.w);
+            l = fmaf(f, ml.y, l);
+          }
+        }
+        const long long row = static_cast<long long>(u.b) * p.hq + u.kvh * G + g;
+        pdl_wait();  // no-op: this kernel is the first of its call
+        reinterpret_cast<float4*>(p.res_o + row * kHeadDim)[d4] = o;
+        if (d4 == 0) p.res_ml[row] = make_float2(M, l);
+      }
+      consumer_sync<NW>();  // the merge buffer is free for the unit's own merge
+    }
+  };
+
   int slot = 0;          // slot of the next stage (stages run in the producers' order)
   uint32_t phase = 0u;   // parity of the slot's current fill
   for (int k = 0; k < n_units; ++k) {
     const UnitStages u = unit_stages<kStageTok>(p, k, clamp_len(ulen_c[k]));
     if (k > 0) consumer_sync<NW>();  // previous unit's merge buffers and q~ are free
+    if constexpr (kResidual) {
+      if (u.s == p.splits - 1) residual_partial(u);
+    }
     if (k > 0) {
       transform_query(k);
       consumer_sync<NW>();
@@ -1465,10 +1582,11 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   __syncthreads();  // matches the producers' final barrier
 }
 
-template <int DK, int BK, int DV, int BV, int NG, int NW, bool kAppend, int kMethod = kMethodGather>
+template <int DK, int BK, int DV, int BV, int NG, int NW, bool kAppend, int kMethod = kMethodGather,
+          bool kResidual = false>
 cudaError_t launch_split(const DecodeParams& p, int grid, size_t smem, cudaStream_t stream,
                          bool overlap) {
-  auto kern = vq_decode_split_kernel<DK, BK, DV, BV, NG, NW, kAppend, kMethod>;
+  auto kern = vq_decode_split_kernel<DK, BK, DV, BV, NG, NW, kAppend, kMethod, kResidual>;
   static SmemOptIn opt_in;
   cudaError_t e = ensure_smem(kern, smem, opt_in);
   if (e != cudaSuccess) return e;
@@ -1487,6 +1605,14 @@ cudaError_t launch_formats(const DecodeParams& p, int grid, size_t smem, cudaStr
         if (method == kMethodBins) return launch_split<4, 8, 4, 8, 4, 12, false, kMethodBins>(p, grid, smem, stream, ov);
       }
     }
+    return cudaErrorInvalidValue;
+  }
+  if (p.residual) {  // attention with the residual window inside: the default shapes only
+    if (p.warps == 12 && !wide)
+      return launch_split<DK, BK, DV, BV, 4, 12, false, kMethodGather, true>(p, grid, smem, stream, ov);
+    if (p.warps == 8)
+      return wide ? launch_split<DK, BK, DV, BV, 8, 8, false, kMethodGather, true>(p, grid, smem, stream, ov)
+                  : launch_split<DK, BK, DV, BV, 4, 8, false, kMethodGather, true>(p, grid, smem, stream, ov);
     return cudaErrorInvalidValue;
   }
   if (p.append) {  // the decode step with the append inside: the default shapes only

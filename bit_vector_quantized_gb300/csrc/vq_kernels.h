@@ -67,6 +67,17 @@ struct DecodeParams {
   const void* v_new;
   uint8_t* k_pool_w;          // the pools, written (k_pool / v_pool as writable pointers)
   uint8_t* v_pool_w;
+  // Full-precision residual window inside the attention kernel (residual != 0):
+  // the unit of each (sequence, KV head)'s last split turns the window's
+  // tokens into one more partial (res_o, res_ml), merged by the combine.
+  int residual;
+  const void* k_res;          // fp16 [B][Hkv][res_capacity][128]
+  const void* v_res;
+  const int32_t* res_lens;    // [B], clamped to [0, res_capacity]
+  int res_capacity;
+  float* res_o;               // fp32 [B * Hq][128]
+  float2* res_ml;             // [B * Hq]: (m, l), log2 domain
+  float res_scale_log2;       // softmax scale * log2(e) (raw q . k)
 };
 
 struct DequantParams {
@@ -95,16 +106,6 @@ struct CombineParams {
   int splits;
 };
 
-struct ResidualParams {
-  const void* q;              // fp16 [B][Hq][128]
-  const void* k_res;          // fp16 [B][Hkv][capacity][128]
-  const void* v_res;
-  const int32_t* res_lens;    // [B], clamped to [0, capacity]
-  float* res_o;               // fp32 [B * Hq][128]
-  float2* res_ml;             // [B * Hq]: (m, l), log2 domain
-  float scale_log2;           // softmax scale * log2(e)
-  int hq, hkv, group, capacity;
-};
 
 constexpr int kProducerWarps = 4;  // TMA-issuing warps (one in four stages each)
 constexpr int kMaxUnitsPerCta = 256;
@@ -127,8 +128,10 @@ struct DecodeShape {
 // centroids of 8 elements) has no replicas: 32 bytes per centroid index, laid
 // out half-major ([tensor][half][code] x 8 bytes).
 struct DecodeSmem {
-  int tab, qt, merge, ml, units, meta, bar, flag, enc, aux, stage, total;
+  int tab, qt, merge, ml, units, meta, bar, flag, enc, aux, res, stage, total;
 };
+
+
 
 // Score and P.V methods of the split kernel (the pages' alternatives):
 //   kMethodGather: scores and P.V from centroid gathers on the tensor cores;
@@ -168,7 +171,7 @@ __host__ __device__ inline int append_scratch_bytes(int warps, int k_sub, int v_
 __host__ __device__ inline DecodeSmem decode_smem(int k_bits, int v_bits, int group, int k_row,
                                                   int v_row, int nstage, int warps, int stage_tok,
                                                   int append_enc = 0, int append_scratch = 0,
-                                                  int method = 0) {
+                                                  int method = 0, int residual = 0) {
   DecodeSmem s;
   int o = 0;
   const int rows = 1 << (k_bits > v_bits ? k_bits : v_bits);
@@ -183,6 +186,7 @@ __host__ __device__ inline DecodeSmem decode_smem(int k_bits, int v_bits, int gr
   s.flag = o; o = align128(o + 16);
   s.enc = o; o = align128(o + append_enc);
   s.aux = o; o = align128(o + (method ? kLutBytes : 0) + (method == 2 ? (1 << v_bits) * 4 * 4 : 0));
+  s.res = o; (void)residual;  // the residual window uses the merge buffer
   s.stage = o; o = align128(o + nstage * stage_tok * (k_row + v_row));
   s.total = o;
   return s;
@@ -252,8 +256,6 @@ cudaError_t launch_decode(const DecodeParams& p, int k_sub, int k_bits, int v_su
                           int method = kMethodGather);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool overlap);
 cudaError_t launch_dequant(const DequantParams& p, int grid_x, cudaStream_t stream);
-cudaError_t launch_residual(const ResidualParams& p, int grid, cudaStream_t stream, bool overlap);
-size_t residual_smem_bytes(int group, int capacity);
 int dequant_tokens_per_cta();
 
 }  // namespace vqk

@@ -342,9 +342,10 @@ vq_status vq_decode_step(const vq_layout* layout, int32_t batch, const void* q, 
  *   res_capacity  1 .. 4096.
  *   workspace     at least vq_decode_residual_workspace_bytes(layout, batch,
  *                 max_seq_len, num_splits, 0) bytes, 256-byte aligned.
- * Three kernels on `stream`: the residual partial (one CTA per sequence and KV
- * head), the split attention over the codes, and the merge, which takes the
- * residual partial as one more split.  Moving tokens from the residual into
+ * Two kernels on `stream`: the split attention over the codes, in which the
+ * work unit of each (sequence, KV head)'s last split also turns the window's
+ * tokens into one more partial, and the merge, which takes that partial as
+ * one more split.  Moving tokens from the residual into
  * the cache (vq_encode_kv) is the caller's policy.  Other arguments and errors
  * as in vq_decode_attention.  A sequence with no token at all gives a zero
  * row.
