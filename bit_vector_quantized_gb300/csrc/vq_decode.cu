@@ -448,7 +448,9 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   int4* meta = reinterpret_cast<int4*>(smem + L.meta);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar);
   uint64_t* empty = full + NS;
-  uint64_t* app_bar = full + 2 * NS;  // fused append: the encoded rows are in the pools
+  float* const enc_kn = reinterpret_cast<float*>(smem + L.enc);  // fused append: ||c||^2 tables
+  float* const enc_vn = enc_kn + (1 << BK);
+  int2* const enc_scr = reinterpret_cast<int2*>(enc_vn + (1 << BV));  // [NP][32][4] argmin scratch
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flag);
   uint8_t* stages = smem + L.stage;
 
@@ -526,7 +528,6 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       mbar_init(full + i, 1);
       mbar_init(empty + i, NW);
     }
-    mbar_init(app_bar, 2);  // consumer warps 0 (K rows) and 1 (V rows)
     mbar_init_fence();
     *abort_flag = 0;
   }
@@ -617,12 +618,92 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       ++cur.j;
       it_seek(cur);
     }
+    // Fused append: the producer warps encode the new token of every unit
+    // the CTA owns one for (append_owned), once the first ring of stages is
+    // on its way (or before the stage holding such a token, whichever comes
+    // first).  Each warp scans a slice of each codebook with the encode
+    // kernel's score arithmetic; warps 0 and 1 merge the slices in index order
+    // (lowest index on ties), pack the K and V rows and store them into the
+    // pools through the page table, fencing the stores for the copy engine.
+    // The stage holding an attended new token is issued only after this.
+    auto encode_phase = [&]() {
+      if constexpr (kAppend) {
+        asm volatile("bar.sync 4, %0;" ::"n"((NW + NP) * 32) : "memory");  // the consumers' table and norms
+        constexpr int NSK = DK == 2 ? 2 : 1, NSV = DV == 2 ? 2 : 1;
+        for (int k = 0; k < n_units; ++k) {
+          const int raw = ulen_p[k];
+          const UnitId id = unit_id(p, k);
+          if (!append_owned(p, id.s, raw)) continue;
+          const int pos = raw - 1;
+          const long long vrow = (static_cast<long long>(id.b) * p.hkv + id.kvh) * kHeadDim;
+          const uint2 rk = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.k_new) + vrow) + lane);
+          const uint2 rv = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.v_new) + vrow) + lane);
+          const float4 lam = __ldg(reinterpret_cast<const float4*>(p.lambda + id.kvh * kHeadDim) + lane);
+          const int pi = pos / P;
+          const int pg = pi < p.max_pages ? __ldg(p.page_table + static_cast<long long>(id.b) * p.max_pages + pi) : -1;
+          float xk[4], xv[4];
+          {
+            const __half2 k01 = *reinterpret_cast<const __half2*>(&rk.x), k23 = *reinterpret_cast<const __half2*>(&rk.y);
+            const __half2 v01 = *reinterpret_cast<const __half2*>(&rv.x), v23 = *reinterpret_cast<const __half2*>(&rv.y);
+            xk[0] = __low2float(k01) / lam.x;  // keys: smoothing, Walsh-Hadamard, 1/sqrt(128)
+            xk[1] = __high2float(k01) / lam.y;
+            xk[2] = __low2float(k23) / lam.z;
+            xk[3] = __high2float(k23) / lam.w;
+            xv[0] = __low2float(v01);
+            xv[1] = __high2float(v01);
+            xv[2] = __low2float(v23);
+            xv[3] = __high2float(v23);
+          }
+          fwht128_warp(xk, lane);
+          const float rs = 0.08838834764831845f;  // 1/sqrt(128)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) xk[e] *= rs;
+          float bk[2], bv[2];
+          int ik[2], iv[2];
+          append_scan<DK>(xk, 0u, enc_kn, (pw << BK) / NP, ((pw + 1) << BK) / NP, bk, ik);
+          append_scan<DV>(xv, 128u, enc_vn, (pw << BV) / NP, ((pw + 1) << BV) / NP, bv, iv);
+          producer_sync<NP>();  // the previous token's scratch has been read
+          int2* scr_k = enc_scr;
+          int2* scr_v = enc_scr + NP * 32 * NSK;
+#pragma unroll
+          for (int t = 0; t < NSK; ++t) scr_k[(pw * 32 + lane) * NSK + t] = make_int2(__float_as_int(bk[t]), ik[t]);
+#pragma unroll
+          for (int t = 0; t < NSV; ++t) scr_v[(pw * 32 + lane) * NSV + t] = make_int2(__float_as_int(bv[t]), iv[t]);
+          producer_sync<NP>();
+          if (pw < 2) {  // warp 0 merges and stores K, warp 1 V
+            int idx[2];
+            if (pw == 0) merge_slices<NSK>(scr_k, NP, lane, idx);
+            else merge_slices<NSV>(scr_v, NP, lane, idx);
+            const uint32_t word = pw == 0 ? pack_row_word<NSK, BK>(idx, lane) : pack_row_word<NSV, BV>(idx, lane);
+            const int rb = pw == 0 ? KROW : VROW;
+            const bool okp = pg >= 0 && pg < p.num_pages;
+            if (!okp && lane == 0 && pw == 0) report(p.status, kDevBadPage);
+            if (okp && lane < rb / 4) {
+              uint8_t* pool = pw == 0 ? p.k_pool_w : p.v_pool_w;
+              const long long r0 = (static_cast<long long>(pg) * p.hkv + id.kvh) * P + pos % P;
+              reinterpret_cast<uint32_t*>(pool + r0 * rb)[lane] = word;
+              fence_proxy_async_global();
+            }
+          }
+        }
+        producer_sync<NP>();  // every new row is stored and fenced before its stage is copied
+      }
+    };
     // the page looked up at entry is this stage's unless the first unit was too short
     int page = (cur.k == 0 && cur.j == pw) ? page_r : lookup(cur);
     pdl_wait();  // the pools may be written by the previous kernel: copy only after it
     int n = pw;
-    bool stop = false, app_ready = false;
+    bool stop = false, encoded = !kAppend;
     while (cur.k < n_units) {
+      if constexpr (kAppend) {
+        if (!encoded) {  // before the first slot wait, or before a stage holding a new token
+          const int t0 = cur.u.t_begin + cur.j * kStageTok;
+          if (n >= NS || append_attended(p, t0, min(t0 + kStageTok, cur.u.t_end), ulen_p[cur.k])) {
+            encode_phase();
+            encoded = true;
+          }
+        }
+      }
       const int slot = n % NS;
       if (n >= NS) {  // wait until the consumers have released the slot
         const uint32_t par = static_cast<uint32_t>(n / NS - 1) & 1u;
@@ -639,30 +720,12 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
           }
         }
       }
-      if (kAppend && !app_ready) {  // the stage holding an appended token waits for its rows
-        const int raw = ulen_p[cur.k];
-        const int t0 = cur.u.t_begin + cur.j * kStageTok;
-        if (append_attended(p, t0, min(t0 + kStageTok, cur.u.t_end), raw)) {
-          bool ok = mbar_try_wait(app_bar, 0u);
-          if (!__all_sync(kFull, ok)) {
-            ok = !*abort_flag && mbar_wait_bounded(app_bar, 0u, abort_flag, p.timeout_ns);
-            if (!__all_sync(kFull, ok)) {
-              if (lane == 0 && !*abort_flag) {
-                *abort_flag = 1;
-                report(p.status, kDevTimeout);
-              }
-              stop = true;
-              break;
-            }
-          }
-          app_ready = true;
-        }
-      }
       issue(cur.u, cur.j, page, n);
       skip(cur);
       page = lookup(cur);
       n += NP;
     }
+    if (!encoded) encode_phase();  // every producer warp takes part once
     __syncthreads();  // every consumer is done
     if (stop && lane == 0) {  // wait (bounded) for this warp's copies still in flight
       for (int i = n - NP; i >= 0 && i >= n - NS - NP; i -= NP) {
@@ -756,8 +819,6 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
 
   // Fused append: ||c||^2 of every centroid in fp32, computed as the encode
   // kernel computes it (a chain of fused multiply-adds in element order).
-  float* const enc_kn = reinterpret_cast<float*>(smem + L.enc);
-  float* const enc_vn = enc_kn + (1 << BK);
   if constexpr (kAppend) {
     {
       auto norms = [&](const uint2 (&cb)[kNB], int n_i, int rows, int d, float* cn) {
@@ -776,6 +837,8 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       norms(cbk_r, kNK, 1 << BK, DK, enc_kn);
       norms(cbv_r, kNV, 1 << BV, DV, enc_vn);
     }
+    // the table and the norms are what the producers' encode reads
+    asm volatile("bar.arrive 4, %0;" ::"n"((NW + NP) * 32) : "memory");
   }
   // q~ = q diag(lambda) H_D * scale * log2(e), split into fp16 hi + lo parts
   // and stored in the score mma's B-operand order: table [head][hi, lo][c][16
@@ -809,89 +872,6 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       }
     }
   };
-  // Fused append: encodes the new token of unit u's (sequence, KV head)
-  // (append_owned).  Every consumer warp scans a slice of each codebook;
-  // warps 0 and 1 merge the slices in index order, pack the K and V rows and
-  // store them into the pools through the page table, each storing lane
-  // fencing its stores for the copy engine (the bulk copies that read them
-  // are issued after the caller's signal on app_bar).
-  auto append_encode = [&](const UnitStages& u, int raw_len) {
-    if constexpr (kAppend) {
-      const int pos = raw_len - 1;
-      constexpr int NSK = DK == 2 ? 2 : 1, NSV = DV == 2 ? 2 : 1;
-      const long long vrow = (static_cast<long long>(u.b) * p.hkv + u.kvh) * kHeadDim;
-      const uint2 rk = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.k_new) + vrow) + lane);
-      const uint2 rv = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.v_new) + vrow) + lane);
-      const float4 lam = __ldg(reinterpret_cast<const float4*>(p.lambda + u.kvh * kHeadDim) + lane);
-      const int pi = pos / p.page_size;
-      const int page = pi < p.max_pages ? __ldg(p.page_table + static_cast<long long>(u.b) * p.max_pages + pi) : -1;
-      float xk[4], xv[4];
-      {
-        const __half2 k01 = *reinterpret_cast<const __half2*>(&rk.x), k23 = *reinterpret_cast<const __half2*>(&rk.y);
-        const __half2 v01 = *reinterpret_cast<const __half2*>(&rv.x), v23 = *reinterpret_cast<const __half2*>(&rv.y);
-        xk[0] = __low2float(k01) / lam.x;  // keys: smoothing, Walsh-Hadamard, 1/sqrt(128)
-        xk[1] = __high2float(k01) / lam.y;
-        xk[2] = __low2float(k23) / lam.z;
-        xk[3] = __high2float(k23) / lam.w;
-        xv[0] = __low2float(v01);
-        xv[1] = __high2float(v01);
-        xv[2] = __low2float(v23);
-        xv[3] = __high2float(v23);
-      }
-      fwht128_warp(xk, lane);
-      const float rs = 0.08838834764831845f;  // 1/sqrt(128)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) xk[e] *= rs;
-      float bk[2], bv[2];
-      int ik[2], iv[2];
-      append_scan<DK>(xk, 0u, enc_kn, (warp << BK) / NW, ((warp + 1) << BK) / NW, bk, ik);
-      append_scan<DV>(xv, 128u, enc_vn, (warp << BV) / NW, ((warp + 1) << BV) / NW, bv, iv);
-      // scratch: K entries [warp][lane][NSK], then V entries [warp][lane][NSV] (score bits, index)
-      int2* scr_k = reinterpret_cast<int2*>(merge);
-      int2* scr_v = scr_k + NW * 32 * NSK;
-#pragma unroll
-      for (int t = 0; t < NSK; ++t) scr_k[(warp * 32 + lane) * NSK + t] = make_int2(__float_as_int(bk[t]), ik[t]);
-#pragma unroll
-      for (int t = 0; t < NSV; ++t) scr_v[(warp * 32 + lane) * NSV + t] = make_int2(__float_as_int(bv[t]), iv[t]);
-      consumer_sync<NW>();
-      if (warp < 2) {  // warp 0 merges and stores K, warp 1 V
-        const int tv = warp;
-        int idx[2];
-        if (tv == 0) merge_slices<NSK>(scr_k, NW, lane, idx);
-        else merge_slices<NSV>(scr_v, NW, lane, idx);
-        const uint32_t word = tv == 0 ? pack_row_word<NSK, BK>(idx, lane) : pack_row_word<NSV, BV>(idx, lane);
-        const int row = tv == 0 ? KROW : VROW;
-        const bool ok = page >= 0 && page < p.num_pages;
-        if (!ok && lane == 0 && tv == 0) report(p.status, kDevBadPage);
-        if (ok && lane < row / 4) {
-          pdl_wait();  // no-op: this kernel is the first of its call
-          uint8_t* pool = tv == 0 ? p.k_pool_w : p.v_pool_w;
-          const long long r0 = (static_cast<long long>(page) * p.hkv + u.kvh) * p.page_size + pos % p.page_size;
-          reinterpret_cast<uint32_t*>(pool + r0 * row)[lane] = word;
-          fence_proxy_async_global();
-        }
-      }
-    }
-  };
-  if constexpr (kAppend) {  // every appended token of the CTA's units, before the first unit starts
-    consumer_sync<NW>();  // ||c||^2 tables visible
-    bool any = false, attended = false;
-    for (int k = 0; k < n_units; ++k) {
-      const int raw = ulen_c[k];
-      const UnitId id = unit_id(p, k);
-      if (!append_owned(p, id.s, raw)) continue;
-      if (any) consumer_sync<NW>();  // the previous encode's scratch has been read
-      const UnitStages u = unit_stages<kStageTok>(p, k, clamp_len(raw));
-      append_encode(u, raw);
-      any = true;
-      attended = attended || append_attended(p, u.t_begin, u.t_end, raw);
-    }
-    if (attended && warp < 2) {  // the rows of the attended appends are in the pools
-      __syncwarp();
-      if (lane == 0) mbar_arrive(app_bar);
-    }
-    consumer_sync<NW>();  // the merge buffer (the encode scratch) is free again
-  }
   transform_query(0);
   consumer_sync<NW>();  // codebook table, unit lengths and the first unit's q~ visible
 

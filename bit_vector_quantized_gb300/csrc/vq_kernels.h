@@ -150,18 +150,16 @@ constexpr int kTabRowWide = 32;   // 1.5-bit format (12-bit codes): K and V cent
 __host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
 
 // Bytes of the fused append's encode tables: per tensor ||c_j||^2 (fp32,
-// 2^bits); then the packed new K and V rows (64 bytes each, at most).  The
-// centroids themselves are read from the replicated fp16 table.
+// 2^bits), then the producer warps' argmin scratch ([4 warps][32 lanes][up to
+// 2 + 2 sub-vectors] x (score, index)).  The centroids themselves are read
+// from the replicated fp16 table.
 __host__ __device__ inline int append_enc_bytes(int k_bits, int v_bits) {
-  return ((1 << k_bits) + (1 << v_bits)) * 4 + 128;
+  return ((1 << k_bits) + (1 << v_bits)) * 4 + 4 * 32 * 4 * 8;
 }
 
-// Bytes of the fused append's argmin scratch: per tensor, warps x 32 lanes x
-// (sub-vectors per lane: 2 for d = 2, else 1) x (score, index); it shares the
-// merge buffer.
-__host__ __device__ inline int append_scratch_bytes(int warps, int k_sub, int v_sub) {
-  return warps * 32 * ((k_sub == 2 ? 2 : 1) + (v_sub == 2 ? 2 : 1)) * 8;
-}
+// Bytes by which the append grows the merge buffer (none: its scratch is in
+// the encode tables' region).
+__host__ __device__ inline int append_scratch_bytes(int, int, int) { return 0; }
 
 // append_enc / append_scratch: the fused append's table and scratch bytes (0: no append)
 // method: a DecodeMethod; the table-based ones keep only the gathered
