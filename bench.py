@@ -77,6 +77,10 @@ def parse():
     ap.add_argument("--methods-only", action="store_true",
                     help="launch the split kernel three times per method on the workload and "
                          "exit (a short program for an ncu capture of the three methods)")
+    ap.add_argument("--launches-only", action="store_true",
+                    help="launch the split kernel alone four times, then the decode step four "
+                         "times, on the workload (seeded random codes) and exit (a short program "
+                         "for ncu captures of either)")
     return ap.parse_args()
 
 
@@ -442,7 +446,7 @@ def layout_row_bytes(w, which):
     return (-(-(w.head_dim // d) * b // 8) + 3) // 4 * 4
 
 
-def split_kernel_block(torch, vq, wi, dev, steps, l2, hbm_peak):
+def split_kernel_block(torch, vq, wi, dev, steps, l2, hbm_peak, only_launch=False):
     """The decode step and the split attention kernel alone on another
     workload, timed like the headline: CUDA graphs of `steps` back-to-back
     calls rotating over cache copies larger than twice L2.  The pools hold
@@ -459,7 +463,7 @@ def split_kernel_block(torch, vq, wi, dev, steps, l2, hbm_peak):
     seq_d = torch.from_numpy(lens).to(dev)
     max_len = int(lens.max())
     step_bytes = code_bytes_per_step(w)
-    copies = max(1, -(-2 * l2 // step_bytes))
+    copies = 1 if only_launch else max(1, -(-2 * l2 // step_bytes))
     gen = torch.Generator(device=dev).manual_seed(1000 + wi)
     krow, vrow = layout_row_bytes(w, "k"), layout_row_bytes(w, "v")
     pools = [(torch.randint(0, 256, (num_pages, w.num_kv_heads, w.page_size, krow), generator=gen,
@@ -489,6 +493,12 @@ def split_kernel_block(torch, vq, wi, dev, steps, l2, hbm_peak):
                           0.0, splits, p(out), p(ws), ws_bytes, p(status),
                           torch.cuda.current_stream().cuda_stream)
 
+    if only_launch:
+        for fn in (split_only, step):
+            for i in range(4):
+                fn(i)
+        torch.cuda.synchronize()
+        return {"workload": w.name, "num_splits": splits, "device_status": int(status.item())}
     split_ms = graph_ms(torch, dev, split_only, steps)
     step_ms = graph_ms(torch, dev, step, steps)
     torch.cuda.synchronize()
@@ -639,6 +649,13 @@ def main():
         r = method_comparison(torch, vq, args.workload, dev, 3, l2, measured_hbm()[0], only_launch=True)
         print(json.dumps({"methods_only": w.name, "device_status": r.get("device_status"),
                           "skipped": r.get("skipped")}), flush=True)
+        return
+    if args.launches_only:
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        r = split_kernel_block(torch, vq, args.workload, dev, 4, l2, measured_hbm()[0],
+                               only_launch=True)
+        print(json.dumps({"launches_only": w.name, **r}), flush=True)
+        assert r["device_status"] == 0, r
         return
     dist = None
     if world > 1:

@@ -375,8 +375,8 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
     int ns = vqk::kMaxStages;
     for (; ns >= vqk::kProducerWarps; --ns) {
       bytes = vqk::decode_smem(L.k_bits, L.v_bits, p.group, p.k_row, p.v_row, ns, sh.warps,
-                               sh.stage_tok(), with_append ? vqk::append_enc_bytes(L.k_bits, L.v_bits) : 0,
-                               with_append ? vqk::append_scratch_bytes(sh.warps, L.k_sub, L.v_sub) : 0,
+                               sh.stage_tok(),
+                               with_append ? vqk::append_enc_bytes(L.k_bits, L.v_bits, L.k_sub, L.v_sub) : 0,
                                method, residual ? 1 : 0)
                   .total;
       if (optin <= 0 || bytes <= static_cast<size_t>(optin)) return ns;
@@ -575,10 +575,11 @@ vq_status vq_decode_step(const vq_layout* layout, int32_t batch, const void* q, 
   // attention kernel (one launch, then the merge) when the attention kernel's
   // shape leaves room for it; the 1.5-bit format appends with the encode
   // kernel first.
-  // One CTA encodes each appended token in its prologue, so the fusion pays
-  // off while there is about one append per CTA; with more, the separate
-  // encode kernel spreads them over the GPU sooner (measured: 32K, ragged
-  // batch-16 and 196K steps faster fused, the batch-64 step slower).
+  // The producer warps of one CTA encode each appended token while their
+  // first copies are in flight, so the fusion pays off while there is about
+  // one append per CTA; with more, the separate encode kernel spreads them
+  // over the GPU sooner (measured: 32K, ragged batch-16 and 196K steps faster
+  // fused, the batch-64 step slower).
   const int sms_now = device_sms();
   bool fused = L.k_bits <= 9 && L.v_bits <= 9 &&
                static_cast<long long>(batch) * L.num_kv_heads <= (sms_now > 0 ? sms_now : 0);

@@ -48,6 +48,18 @@
 //     the lane with lane / 4 = r accumulates output dims 16r .. 16r + 15 for V.
 //   * Each stage's scores and the previous stage's P.V form one basic block, so
 //     the two mma chains, their gathers and the softmax bookkeeping overlap.
+//   * Compile-time variants of the same kernel:
+//       - kAppend (the decode step in one launch): the producer warps encode
+//         the new token of each (sequence, KV head) whose split the CTA owns,
+//         with the encode kernel's arithmetic, while their first copies are
+//         in flight, store the packed rows and fence them for the copy
+//         engine; the stage holding the token is copied after that.
+//       - kMethod: the pages' other score and P.V forms (a per-query lookup
+//         table of q~ x C_k for the scores; P.V through per-code bins), for
+//         measurement against the gather form.
+//       - kResidual: the unit of a (sequence, KV head)'s last split also
+//         turns a full-precision window of recent tokens into one more
+//         partial, before its stages.
 //   * Every mbarrier wait is bounded (%globaltimer); on a timeout the CTA
 //     raises an abort flag, drains its copies in flight and reports
 //     VQ_DEV_TIMEOUT.  Launch ordering follows pdl_wait in vq_device.cuh.
@@ -316,60 +328,78 @@ __device__ __forceinline__ int piece_lo(int t0, int lane, int l2) {
 // kernel forms it (the same fused multiply-adds, in the same order, on the same
 // fp32 -2 c and ||c||^2 values), and a strict '<' in index order keeps the
 // lowest index among equal scores, so the codes are those of vq_encode_kv.
+// cm: the fp32 -2 c table [code][D]; cn: ||c||^2 [code].
 template <int D>
-__device__ __forceinline__ void append_scan(const float (&x)[4], uint32_t half, const float* cn,
+__device__ __forceinline__ void append_scan(const float (&x)[4], const float* cm, const float* cn,
                                             int j0, int j1, float (&best)[2], int (&idx)[2]) {
-  // centroid j: replica 0 of its table row (fp16); -2 c is exact in fp32
+  static_assert(D == 2 || D == 4, "sub-vector length 2 or 4");
   best[0] = best[1] = INFINITY;
   idx[0] = idx[1] = 0x7fffffff;
-  if constexpr (D == 4) {
-    auto score = [&](int j) {
-      const uint2 w = tab64((static_cast<uint32_t>(j) << 8) | half);
-      const __half2 c01 = *reinterpret_cast<const __half2*>(&w.x), c23 = *reinterpret_cast<const __half2*>(&w.y);
-      float sc = cn[j];
-      sc = fmaf(x[0], -2.f * __low2float(c01), sc);
-      sc = fmaf(x[1], -2.f * __high2float(c01), sc);
-      sc = fmaf(x[2], -2.f * __low2float(c23), sc);
-      return fmaf(x[3], -2.f * __high2float(c23), sc);
-    };
-    int j = j0;
-    for (; j + 4 <= j1; j += 4) {
-      float sc[4];
+  // the scan runs beside the streaming consumer warps, whose gathers keep the
+  // shared-memory pipe busy: the loads of kU centroids go out before any use
+  constexpr int kU = 8;
+  auto group = [&](int j, int u_n) {
+    float c[kU][D], n[kU];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) sc[u] = score(j + u);
+    for (int u = 0; u < kU; ++u) {
+      if (u >= u_n) break;
+      if constexpr (D == 4) {
+        const float4 v = reinterpret_cast<const float4*>(cm)[j + u];
+        c[u][0] = v.x; c[u][1] = v.y; c[u][2] = v.z; c[u][3] = v.w;
+      } else {
+        const float2 v = reinterpret_cast<const float2*>(cm)[j + u];
+        c[u][0] = v.x; c[u][1] = v.y;
+      }
+      n[u] = cn[j + u];
+    }
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (sc[u] < best[0]) {
-          best[0] = sc[u];
+    for (int u = 0; u < kU; ++u) {
+      if (u >= u_n) break;
+      if constexpr (D == 4) {
+        float sc = fmaf(x[0], c[u][0], n[u]);
+        sc = fmaf(x[1], c[u][1], sc);
+        sc = fmaf(x[2], c[u][2], sc);
+        sc = fmaf(x[3], c[u][3], sc);
+        if (sc < best[0]) {
+          best[0] = sc;
           idx[0] = j + u;
         }
-    }
-    for (; j < j1; ++j) {
-      const float sc = score(j);
-      if (sc < best[0]) {
-        best[0] = sc;
-        idx[0] = j;
+      } else {
+        const float s0 = fmaf(x[1], c[u][1], fmaf(x[0], c[u][0], n[u]));
+        const float s1 = fmaf(x[3], c[u][1], fmaf(x[2], c[u][0], n[u]));
+        if (s0 < best[0]) {
+          best[0] = s0;
+          idx[0] = j + u;
+        }
+        if (s1 < best[1]) {
+          best[1] = s1;
+          idx[1] = j + u;
+        }
       }
     }
-  } else {
-    static_assert(D == 2, "sub-vector length 2 or 4");
-    for (int j = j0; j < j1; ++j) {
-      const uint32_t w = tab32((static_cast<uint32_t>(j) << 8) | half);
-      const __half2 c01 = *reinterpret_cast<const __half2*>(&w);
-      const float cx = -2.f * __low2float(c01), cy = -2.f * __high2float(c01);
-      const float n = cn[j];
-      const float s0 = fmaf(x[1], cy, fmaf(x[0], cx, n));
-      const float s1 = fmaf(x[3], cy, fmaf(x[2], cx, n));
-      if (s0 < best[0]) {
-        best[0] = s0;
-        idx[0] = j;
-      }
-      if (s1 < best[1]) {
-        best[1] = s1;
-        idx[1] = j;
-      }
-    }
-  }
+  };
+  int j = j0;
+  for (; j + kU <= j1; j += kU) group(j, kU);
+  for (; j < j1; ++j) group(j, 1);
+}
+
+// ||c_j||^2 and -2 c_j in fp32 for the fused append's scan, as the encode
+// kernel forms them: the norm a chain of fused multiply-adds in element
+// order, -2 c exact.  w holds the fp16 centroid (its first D elements).
+template <int D>
+__device__ __forceinline__ void append_tables(uint2 w, int j, float* cn, float* cm) {
+  const __half2 h01 = *reinterpret_cast<const __half2*>(&w.x);
+  const __half2 h23 = *reinterpret_cast<const __half2*>(&w.y);
+  const float v[4] = {__low2float(h01), __high2float(h01), D == 4 ? __low2float(h23) : 0.f,
+                      D == 4 ? __high2float(h23) : 0.f};
+  float n = 0.f;
+#pragma unroll
+  for (int e = 0; e < D; ++e) n = fmaf(v[e], v[e], n);
+  cn[j] = n;
+  if constexpr (D == 4)
+    reinterpret_cast<float4*>(cm)[j] = make_float4(-2.f * v[0], -2.f * v[1], -2.f * v[2], -2.f * v[3]);
+  else
+    reinterpret_cast<float2*>(cm)[j] = make_float2(-2.f * v[0], -2.f * v[1]);
 }
 
 // Merges the warps' argmin slices of one tensor, held as (score bits, index)
@@ -436,8 +466,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   constexpr bool kLut = kMethod == kMethodLut, kBins = kMethod == kMethodBins;
   static_assert(!kResidual || (kMethod == kMethodGather && !kAppend), "the residual window runs alone");
   const DecodeSmem L = decode_smem(BK, BV, G, KROW, VROW, NS, NW, kStageTok,
-                                   kAppend ? append_enc_bytes(BK, BV) : 0,
-                                   kAppend ? append_scratch_bytes(NW, DK, DV) : 0, kMethod,
+                                   kAppend ? append_enc_bytes(BK, BV, DK, DV) : 0, kMethod,
                                    kResidual ? 1 : 0);
   float* qt = reinterpret_cast<float*>(smem + L.qt);
   // the LUT method's merge buffer shares the LUT (built again for every unit)
@@ -450,7 +479,9 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   uint64_t* empty = full + NS;
   float* const enc_kn = reinterpret_cast<float*>(smem + L.enc);  // fused append: ||c||^2 tables
   float* const enc_vn = enc_kn + (1 << BK);
-  int2* const enc_scr = reinterpret_cast<int2*>(enc_vn + (1 << BV));  // [NP][32][4] argmin scratch
+  float* const enc_km = enc_vn + (1 << BV);                          // -2 c tables (fp32)
+  float* const enc_vm = enc_km + (1 << BK) * DK;
+  int2* const enc_scr = reinterpret_cast<int2*>(enc_vm + (1 << BV) * DV);  // [NP][32][4] argmin scratch
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flag);
   uint8_t* stages = smem + L.stage;
 
@@ -660,8 +691,8 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
           for (int e = 0; e < 4; ++e) xk[e] *= rs;
           float bk[2], bv[2];
           int ik[2], iv[2];
-          append_scan<DK>(xk, 0u, enc_kn, (pw << BK) / NP, ((pw + 1) << BK) / NP, bk, ik);
-          append_scan<DV>(xv, 128u, enc_vn, (pw << BV) / NP, ((pw + 1) << BV) / NP, bv, iv);
+          append_scan<DK>(xk, enc_km, enc_kn, (pw << BK) / NP, ((pw + 1) << BK) / NP, bk, ik);
+          append_scan<DV>(xv, enc_vm, enc_vn, (pw << BV) / NP, ((pw + 1) << BV) / NP, bv, iv);
           producer_sync<NP>();  // the previous token's scratch has been read
           int2* scr_k = enc_scr;
           int2* scr_v = enc_scr + NP * 32 * NSK;
@@ -817,25 +848,19 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   }
   if (tid < n_units) ulen_c[tid] = len_r[0];  // raw: the append needs the unclamped length
 
-  // Fused append: ||c||^2 of every centroid in fp32, computed as the encode
-  // kernel computes it (a chain of fused multiply-adds in element order).
+  // Fused append: ||c||^2 and -2 c of every centroid in fp32, computed as the
+  // encode kernel computes them (the norm a chain of fused multiply-adds in
+  // element order; -2 c exact).
   if constexpr (kAppend) {
-    {
-      auto norms = [&](const uint2 (&cb)[kNB], int n_i, int rows, int d, float* cn) {
 #pragma unroll
-        for (int i = 0; i < kNB; ++i) {
-          const int j = tid + i * kConsumerThreads;
-          if (i >= n_i || j >= rows) break;
-          const __half2 h01 = *reinterpret_cast<const __half2*>(&cb[i].x);
-          const __half2 h23 = *reinterpret_cast<const __half2*>(&cb[i].y);
-          const float v[4] = {__low2float(h01), __high2float(h01), __low2float(h23), __high2float(h23)};
-          float n = 0.f;
-          for (int e = 0; e < d; ++e) n = fmaf(v[e], v[e], n);
-          cn[j] = n;
-        }
-      };
-      norms(cbk_r, kNK, 1 << BK, DK, enc_kn);
-      norms(cbv_r, kNV, 1 << BV, DV, enc_vn);
+    for (int i = 0; i < kNK; ++i) {
+      const int j = tid + i * kConsumerThreads;
+      if (j < (1 << BK)) append_tables<DK>(cbk_r[i], j, enc_kn, enc_km);
+    }
+#pragma unroll
+    for (int i = 0; i < kNV; ++i) {
+      const int j = tid + i * kConsumerThreads;
+      if (j < (1 << BV)) append_tables<DV>(cbv_r[i], j, enc_vn, enc_vm);
     }
     // the table and the norms are what the producers' encode reads
     asm volatile("bar.arrive 4, %0;" ::"n"((NW + NP) * 32) : "memory");
@@ -883,7 +908,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   uint32_t qa[8][2];  // score B operands: NG == 4: columns (2g: hi, 2g+1: lo); NG == 8: hi
   uint32_t qb[8][2];  // NG == 8: lo
   float O[8][4];      // output accumulators (NG == 4 uses O[0..3])
-  float m_run[NGL], l_run[NGL];
+  float m_run[NGL], l_run[NGL] = {};
 
   // ---- code registers -------------------------------------------------------
   // K: tokens r and r+8 of the warp's chunk.  V (G <= 4): tokens c, c+4, c+8,

@@ -150,33 +150,29 @@ constexpr int kTabRowWide = 32;   // 1.5-bit format (12-bit codes): K and V cent
 __host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
 
 // Bytes of the fused append's encode tables: per tensor ||c_j||^2 (fp32,
-// 2^bits), then the producer warps' argmin scratch ([4 warps][32 lanes][up to
-// 2 + 2 sub-vectors] x (score, index)).  The centroids themselves are read
-// from the replicated fp16 table.
-__host__ __device__ inline int append_enc_bytes(int k_bits, int v_bits) {
-  return ((1 << k_bits) + (1 << v_bits)) * 4 + 4 * 32 * 4 * 8;
+// 2^bits), then -2 c_j in fp32 (2^bits x sub, K then V), then the producer
+// warps' argmin scratch ([4 warps][32 lanes][up to 2 + 2 sub-vectors] x
+// (score, index)).
+__host__ __device__ inline int append_enc_bytes(int k_bits, int v_bits, int k_sub, int v_sub) {
+  return ((1 << k_bits) + (1 << v_bits)) * 4 + ((1 << k_bits) * k_sub + (1 << v_bits) * v_sub) * 4 +
+         4 * 32 * 4 * 8;
 }
 
-// Bytes by which the append grows the merge buffer (none: its scratch is in
-// the encode tables' region).
-__host__ __device__ inline int append_scratch_bytes(int, int, int) { return 0; }
-
-// append_enc / append_scratch: the fused append's table and scratch bytes (0: no append)
+// append_enc: the fused append's table and scratch bytes (0: no append)
 // method: a DecodeMethod; the table-based ones keep only the gathered
 // tensor's centroids in the replicated table (128-byte rows), the LUT or the
 // bins in `aux` (the LUT method's merge buffer shares it), and the bins
 // method's fp32 V codebook after them.
 __host__ __device__ inline DecodeSmem decode_smem(int k_bits, int v_bits, int group, int k_row,
                                                   int v_row, int nstage, int warps, int stage_tok,
-                                                  int append_enc = 0, int append_scratch = 0,
-                                                  int method = 0, int residual = 0) {
+                                                  int append_enc = 0, int method = 0, int residual = 0) {
   DecodeSmem s;
   int o = 0;
   const int rows = 1 << (k_bits > v_bits ? k_bits : v_bits);
   s.tab = o; o = align128(o + rows * (k_bits == 12 ? kTabRowWide : method ? kTabRow / 2 : kTabRow));
   s.qt = o; o = align128(o + (group > 4 ? 8 : 4) * 128 * 4);  // q~ operand table, 4 or 8 heads
   const int merge = method ? 0 : warps * group * 128 * 4;
-  s.merge = o; o = align128(o + (merge > append_scratch ? merge : append_scratch));
+  s.merge = o; o = align128(o + merge);
   s.ml = o; o = align128(o + warps * (group > 4 ? 8 : 4) * 8);
   s.units = o; o = align128(o + 2 * kMaxUnitsPerCta * 4);  // consumer and producer copies
   s.meta = o; o = align128(o + nstage * 16);

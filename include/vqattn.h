@@ -296,9 +296,10 @@ vq_status vq_decode_partial_method(const vq_layout* layout, int32_t batch, const
  * bit for bit:
  *   - with at most one sequence-KV-head pair per SM and a format whose codes
  *     are at most 9 bits (every format but the 1.5-bit one), the attention
- *     kernel itself encodes each new token (the CTA whose split holds it
- *     encodes it before its first stage and stores the codes; the stage that
- *     holds the token is copied after the store), then the merge: two kernels
+ *     kernel itself encodes each new token (the producer warps of the CTA
+ *     whose split holds it encode it while their first copies are in flight
+ *     and store the codes; the stage that holds the token is copied only
+ *     after the store), then the merge: two kernels
  *     (the fused append of HACK's decode kernel and of VecInfer's 注意力机制中的
  *     向量量化KV缓存, where the new code joins the cached ones);
  *   - otherwise three kernels: the append encode, the split attention (it
