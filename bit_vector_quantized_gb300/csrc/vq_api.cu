@@ -302,7 +302,7 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
                          float softmax_scale, int32_t num_splits, const void* workspace,
                          size_t workspace_bytes, int32_t* status, vqk::DecodeParams& p,
                          int& grid, size_t& smem, bool* append = nullptr,
-                         int method = vqk::kMethodGather, bool residual = false) {
+                         int method = vqk::kMethodGather, int res_capacity = 0) {
   const vq_layout& L = *layout;
   const void* ptrs[] = {q, lambda, codebook_k, codebook_v, k_pool, v_pool, page_table, seq_lens, workspace};
   const char* names[] = {"q", "lambda", "codebook_k", "codebook_v", "k_pool", "v_pool",
@@ -362,6 +362,10 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
   p.v_row = static_cast<int>(vq_code_row_bytes(L.head_dim, L.v_sub, L.v_bits));
   const float scale = softmax_scale == 0.f ? 1.f / std::sqrt(static_cast<float>(L.head_dim)) : softmax_scale;
   p.qscale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 / std::sqrt(128.0));
+  // residual window: a unit's slice is at most ceil(capacity / splits)
+  // tokens, staged in shared memory up to kMaxResTok at a time
+  const int res_tok = res_capacity > 0 ? std::min((res_capacity + splits - 1) / splits, vqk::kMaxResTok) : 0;
+  p.res_tok = res_tok;
 
   const int optin = device_smem_optin();
   // Pipeline stages: the most (up to kMaxStages) that fit, and never fewer
@@ -377,7 +381,7 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
       bytes = vqk::decode_smem(L.k_bits, L.v_bits, p.group, p.k_row, p.v_row, ns, sh.warps,
                                sh.stage_tok(),
                                with_append ? vqk::append_enc_bytes(L.k_bits, L.v_bits, L.k_sub, L.v_sub) : 0,
-                               method, residual ? 1 : 0)
+                               method, res_tok)
                   .total;
       if (optin <= 0 || bytes <= static_cast<size_t>(optin)) return ns;
     }
@@ -440,23 +444,9 @@ vq_status launch_partial(const vq_layout& L, const vqk::DecodeParams& p, int gri
   return VQ_OK;
 }
 
-// Residual partials after the split partials of the same workspace.
-struct ResLayout {
-  size_t o_off, ml_off, total;
-};
-
-ResLayout res_layout(const vq_layout& L, int batch, int splits) {
-  ResLayout r;
-  const size_t rows = static_cast<size_t>(batch) * L.num_q_heads;
-  r.o_off = ws_layout(L, batch, splits).total;
-  r.ml_off = r.o_off + ((rows * L.head_dim * sizeof(float) + 255) & ~size_t(255));
-  r.total = r.ml_off + ((rows * 2 * sizeof(float) + 255) & ~size_t(255));
-  return r;
-}
-
 vq_status combine_impl(const vq_layout* layout, int32_t batch, int32_t max_seq_len,
                        int32_t num_splits, const void* workspace, size_t workspace_bytes,
-                       void* out, void* stream, bool overlap, bool residual = false) {
+                       void* out, void* stream, bool overlap) {
   const vq_layout& L = *layout;
   if (!workspace || !out) return fail(VQ_ERR_INVALID_ARG, "workspace or out is NULL");
   if (!aligned16(workspace) || !aligned16(out))
@@ -475,13 +465,6 @@ vq_status combine_impl(const vq_layout* layout, int32_t batch, int32_t max_seq_l
   const uint8_t* wsb = static_cast<const uint8_t*>(workspace);
   cp.ws_o = reinterpret_cast<const float*>(wsb + ws.o_off);
   cp.ws_ml = reinterpret_cast<const float2*>(wsb + ws.ml_off);
-  if (residual) {
-    const ResLayout r = res_layout(L, batch, splits);
-    if (workspace_bytes < r.total)
-      return fail(VQ_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, r.total);
-    cp.res_o = reinterpret_cast<const float*>(wsb + r.o_off);
-    cp.res_ml = reinterpret_cast<const float2*>(wsb + r.ml_off);
-  }
   cp.out = out;
   cp.rows = batch * L.num_q_heads;
   cp.splits = splits;
@@ -782,7 +765,7 @@ size_t vq_decode_residual_workspace_bytes(const vq_layout* layout, int32_t batch
   int splits = num_splits;
   if (splits <= 0) splits = vq_default_num_splits(layout, batch, max_seq_len, num_sms);
   if (splits <= 0 || splits > kMaxSplits) return 0;
-  return res_layout(*layout, batch, splits).total;
+  return ws_layout(*layout, batch, splits).total;
 }
 
 vq_status vq_decode_attention_residual(const vq_layout* layout, int32_t batch, const void* q,
@@ -815,28 +798,22 @@ vq_status vq_decode_attention_residual(const vq_layout* layout, int32_t batch, c
   st = prepare_decode(layout, batch, q, lambda, codebook_k, codebook_v, k_pool, v_pool, num_pages,
                       page_table, max_pages_per_seq, seq_lens, max_seq_len, softmax_scale,
                       num_splits, workspace, workspace_bytes, status, p, grid, smem, nullptr,
-                      vqk::kMethodGather, true);
+                      vqk::kMethodGather, res_capacity);
   if (st != VQ_OK) return st;
-  const ResLayout r = res_layout(L, batch, p.splits);
-  if (workspace_bytes < r.total)
-    return fail(VQ_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, r.total);
 
-  // 1. split attention over the codes with the residual window's partial
-  // computed inside (by the unit of each pair's last split), 2. merge
-  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  // 1. split attention over the codes, every unit merging its slice of the
+  // residual window into its own partial, 2. merge of the splits
   p.residual = 1;
   p.k_res = k_res;
   p.v_res = v_res;
   p.res_lens = res_lens;
   p.res_capacity = res_capacity;
-  p.res_o = reinterpret_cast<float*>(wsb + r.o_off);
-  p.res_ml = reinterpret_cast<float2*>(wsb + r.ml_off);
   const float scale = softmax_scale == 0.f ? 1.f / std::sqrt(static_cast<float>(L.head_dim)) : softmax_scale;
   p.res_scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   st = launch_partial(L, p, grid, smem, stream, false);
   if (st != VQ_OK) return st;
   return combine_impl(layout, batch, max_seq_len, p.splits, workspace, workspace_bytes, out, stream,
-                      true, true);
+                      true);
 }
 
 }  // extern "C"

@@ -4,8 +4,7 @@
 // 方法细节 "细粒度分块计算": a (batch, heads, splits) decomposition); every split
 // leaves a partial (m_s, l_s, o_s) in the log2 domain, and the merge is the
 // running-max / running-sum recurrence of the online softmax (相关工作 -
-// FlashAttention) applied across splits.  A full-precision residual window
-// (vq_residual.cu) adds one more partial per row, merged after the splits.
+// FlashAttention) applied across splits.
 #include "vq_device.cuh"
 #include "vq_kernels.h"
 
@@ -25,10 +24,8 @@ __global__ void __launch_bounds__(kHeadDim) vq_combine_kernel(const CombineParam
   pdl_wait();
   const float2* ml = p.ws_ml + static_cast<long long>(row) * p.splits;
   const float* o = p.ws_o + static_cast<long long>(row) * p.splits * kHeadDim + d;
-  // terms: the splits, then the residual partial when there is one
-  const int terms = p.splits + (p.res_ml ? 1 : 0);
   float M = -INFINITY, acc = 0.f, l = 0.f;
-  for (int s0 = 0; s0 < terms; s0 += kC) {
+  for (int s0 = 0; s0 < p.splits; s0 += kC) {
     float2 v[kC];
     float ov[kC];
 #pragma unroll
@@ -39,9 +36,6 @@ __global__ void __launch_bounds__(kHeadDim) vq_combine_kernel(const CombineParam
       if (sp < p.splits) {
         v[i] = __ldcg(ml + sp);
         ov[i] = __ldcg(o + static_cast<long long>(sp) * kHeadDim);
-      } else if (sp < terms) {
-        v[i] = __ldcg(p.res_ml + row);
-        ov[i] = __ldcg(p.res_o + static_cast<long long>(row) * kHeadDim + d);
       }
     }
     float Mc = M;
@@ -68,7 +62,7 @@ __global__ void __launch_bounds__(kHeadDim) vq_combine_kernel(const CombineParam
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool overlap) {
   if (p.rows == 0) return cudaSuccess;
   // chunk of partials loaded at once: the smallest of 4, 8, 16, 32 that holds them all
-  const int terms = p.splits + (p.res_ml ? 1 : 0);
+  const int terms = p.splits;
   auto kern = terms <= 4 ? vq_combine_kernel<4> : terms <= 8 ? vq_combine_kernel<8>
             : terms <= 16 ? vq_combine_kernel<16> : vq_combine_kernel<32>;
   cudaError_t e = launch_pdl(kern, dim3(p.rows), dim3(kHeadDim), 0, stream, p, overlap);

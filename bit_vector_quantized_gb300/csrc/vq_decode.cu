@@ -57,9 +57,9 @@
 //       - kMethod: the pages' other score and P.V forms (a per-query lookup
 //         table of q~ x C_k for the scores; P.V through per-code bins), for
 //         measurement against the gather form.
-//       - kResidual: the unit of a (sequence, KV head)'s last split also
-//         turns a full-precision window of recent tokens into one more
-//         partial, before its stages.
+//       - kResidual: every unit also merges its share of a full-precision
+//         window of recent tokens (prefetched with cp.async while its stages
+//         stream) into its own online softmax.
 //   * Every mbarrier wait is bounded (%globaltimer); on a timeout the CTA
 //     raises an abort flag, drains its copies in flight and reports
 //     VQ_DEV_TIMEOUT.  Launch ordering follows pdl_wait in vq_device.cuh.
@@ -467,13 +467,14 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   static_assert(!kResidual || (kMethod == kMethodGather && !kAppend), "the residual window runs alone");
   const DecodeSmem L = decode_smem(BK, BV, G, KROW, VROW, NS, NW, kStageTok,
                                    kAppend ? append_enc_bytes(BK, BV, DK, DV) : 0, kMethod,
-                                   kResidual ? 1 : 0);
+                                   kResidual ? p.res_tok : 0);
   float* qt = reinterpret_cast<float*>(smem + L.qt);
   // the LUT method's merge buffer shares the LUT (built again for every unit)
   float* merge = reinterpret_cast<float*>(smem + (kLut ? L.aux : L.merge));
   float2* mlbuf = reinterpret_cast<float2*>(smem + L.ml);
   int* ulen_c = reinterpret_cast<int*>(smem + L.units);  // unit lengths, consumers' copy
   int* ulen_p = ulen_c + kMaxUnitsPerCta;                  // producers' copy
+  int* ures_c = ulen_p + kMaxUnitsPerCta;                  // residual window lengths (kResidual)
   int4* meta = reinterpret_cast<int4*>(smem + L.meta);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar);
   uint64_t* empty = full + NS;
@@ -536,7 +537,11 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
         else cbv_r[i].x = __ldg(reinterpret_cast<const uint32_t*>(p.cb_v) + j);
       }
     }
-    if (tid < n_units) len_r[0] = __ldg(p.seq_lens + unit_id(p, tid).b);
+    if (tid < n_units) {
+      const int b = unit_id(p, tid).b;
+      len_r[0] = __ldg(p.seq_lens + b);
+      if constexpr (kResidual) len_r[1] = __ldg(p.res_lens + b);
+    }
     load_q(0);
   } else {
     const int ptid = tid - NW * 32, pw = warp - NW;
@@ -846,7 +851,10 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       fill(cbv_r, kNV, 1 << BV, DV, 128u);
     }
   }
-  if (tid < n_units) ulen_c[tid] = len_r[0];  // raw: the append needs the unclamped length
+  if (tid < n_units) {
+    ulen_c[tid] = len_r[0];  // raw: the append needs the unclamped length
+    if constexpr (kResidual) ures_c[tid] = min(max(len_r[1], 0), p.res_capacity);
+  }
 
   // Fused append: ||c||^2 and -2 c of every centroid in fp32, computed as the
   // encode kernel computes them (the norm a chain of fused multiply-adds in
@@ -1248,23 +1256,37 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
     }
   };
 
-  // Full-precision residual window (VecInfer, 实验结果 / 实验设置: the most
-  // recent tokens stay unquantized): the unit of a (sequence, KV head)'s last
-  // split turns the window's R tokens into one more partial in the log2
-  // domain of the split partials, s = q . k * scale * log2(e) with the raw
-  // query and keys.  Warp w takes tokens w, w + NW, ... (kRB of its rows in
-  // flight at a time) with an online softmax
-  // per head (lane l holds elements 4l .. 4l+3 of the key, the value and the
-  // sum of p v); the warps' partials merge through the merge buffer.
-  auto residual_partial = [&](const UnitStages& u) {
+  // Copies window tokens [t0, t0 + n) of the unit's (sequence, KV head) to
+  // the window area of shared memory (K rows at 0, V rows at res_tok * 256,
+  // then the raw queries when with_q), 16 bytes per cp.async.
+  auto res_issue = [&](const UnitStages& u, int t0, int n, bool with_q) {
     if constexpr (kResidual) {
-      int R = __ldg(p.res_lens + u.b);
-      R = R < 0 ? 0 : (R > p.res_capacity ? p.res_capacity : R);
       const long long head = static_cast<long long>(u.b) * p.hkv + u.kvh;
-      const uint2* kr = reinterpret_cast<const uint2*>(static_cast<const __half*>(p.k_res) +
-                                                       head * p.res_capacity * kHeadDim);
-      const uint2* vr = reinterpret_cast<const uint2*>(static_cast<const __half*>(p.v_res) +
-                                                       head * p.res_capacity * kHeadDim);
+      const uint8_t* kr = static_cast<const uint8_t*>(p.k_res) + (head * p.res_capacity + t0) * (kHeadDim * 2);
+      const uint8_t* vr = static_cast<const uint8_t*>(p.v_res) + (head * p.res_capacity + t0) * (kHeadDim * 2);
+      const uint8_t* qr = static_cast<const uint8_t*>(p.q) + (static_cast<long long>(u.b) * p.hq + u.kvh * G) * (kHeadDim * 2);
+      const int nk = n * 16;  // 16-byte pieces of the K (then V) rows
+      const int total = 2 * nk + (with_q ? G * 16 : 0);
+      for (int i = tid; i < total; i += kConsumerThreads) {
+        const uint8_t* src = i < nk ? kr + i * 16 : i < 2 * nk ? vr + (i - nk) * 16 : qr + (i - 2 * nk) * 16;
+        const int off = i < nk ? i * 16 : i < 2 * nk ? p.res_tok * 256 + (i - nk) * 16 : 2 * p.res_tok * 256 + (i - 2 * nk) * 16;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem + L.res + off)), "l"(src)
+                     : "memory");
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+  };
+
+  // The unit's window slice (see the unit loop) joins the warp's online
+  // softmax: warp w takes slice tokens w, w + NW, ...; every lane forms the G
+  // dot products from its four elements and a butterfly reduction, then lane
+  // (r, c) updates its heads' running maximum, sum and output elements.
+  auto residual_merge = [&](int t0, int n, const UnitStages& u) {
+    if constexpr (kResidual) {
+      const int T = p.res_tok;
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      consumer_sync<NW>();  // every thread's copies are visible
+      const uint8_t* rs = smem + L.res;
       auto unpack = [](uint2 w, float (&f)[4]) {
         const __half2 lo = *reinterpret_cast<const __half2*>(&w.x), hi = *reinterpret_cast<const __half2*>(&w.y);
         f[0] = __low2float(lo);
@@ -1272,91 +1294,109 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
         f[2] = __low2float(hi);
         f[3] = __high2float(hi);
       };
-      float qv[NG][4], acc[NG][4], mr[NG], lr[NG];
+      float qv[NG][4];
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
-        mr[g] = -INFINITY;
-        lr[g] = 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) qv[g][e] = acc[g][e] = 0.f;
-        if (g < G) {
-          float f[4];
-          unpack(__ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.q) +
-                                                     (static_cast<long long>(u.b) * p.hq + u.kvh * G + g) * kHeadDim) +
-                       lane),
-                 f);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) qv[g][e] = f[e] * p.res_scale_log2;
-        }
+        if (g < G) unpack(reinterpret_cast<const uint2*>(rs + 2 * T * 256 + g * 256)[lane], qv[g]);
+        else qv[g][0] = qv[g][1] = qv[g][2] = qv[g][3] = 0.f;
       }
-      constexpr int kRB = 4;  // tokens per warp whose rows are in flight together
-      for (int t0 = warp; t0 < R; t0 += kRB * NW) {
-        uint2 kk[kRB], vv[kRB];
+      // one window token: its G scores (the reductions side by side; heads
+      // >= G have q = 0 and get -inf), then the lane's heads' softmax state
+      // and outputs
+      auto token = [&](const uint8_t* kr, const uint8_t* vr) {
+        float kf[4];
+        unpack(reinterpret_cast<const uint2*>(kr)[lane], kf);
+        float sg[NG];
 #pragma unroll
-        for (int i = 0; i < kRB; ++i) {
-          const int t = t0 + i * NW;
-          kk[i] = t < R ? __ldg(kr + static_cast<long long>(t) * (kHeadDim / 4) + lane) : make_uint2(0u, 0u);
-          vv[i] = t < R ? __ldg(vr + static_cast<long long>(t) * (kHeadDim / 4) + lane) : make_uint2(0u, 0u);
+        for (int g = 0; g < NG; ++g) {
+          sg[g] = qv[g][0] * kf[0];
+          sg[g] = fmaf(qv[g][1], kf[1], sg[g]);
+          sg[g] = fmaf(qv[g][2], kf[2], sg[g]);
+          sg[g] = fmaf(qv[g][3], kf[3], sg[g]);
         }
 #pragma unroll
-        for (int i = 0; i < kRB; ++i) {
-          if (t0 + i * NW >= R) break;  // uniform over the warp
-          float kf[4], vf[4];
-          unpack(kk[i], kf);
-          unpack(vv[i], vf);
+        for (int o = 16; o >= 1; o >>= 1)
 #pragma unroll
-          for (int g = 0; g < NG; ++g) {
-            if (g >= G) break;
-            float a = qv[g][0] * kf[0];
-            a = fmaf(qv[g][1], kf[1], a);
-            a = fmaf(qv[g][2], kf[2], a);
-            a = fmaf(qv[g][3], kf[3], a);
+          for (int g = 0; g < NG; ++g) sg[g] += __shfl_xor_sync(kFull, sg[g], o);
 #pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) a += __shfl_xor_sync(kFull, a, o);
-            const float mn = fmaxf(mr[g], a);
-            const float al = fast_exp2(mr[g] - mn);  // 0 from -inf
-            const float pr = fast_exp2(a - mn);
-            lr[g] = fmaf(lr[g], al, pr);
+        for (int g = 0; g < NG; ++g) sg[g] = g < G ? sg[g] * p.res_scale_log2 : -INFINITY;
+        float s[NGL];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[g][e] = fmaf(acc[g][e], al, pr * vf[e]);
-            mr[g] = mn;
+        for (int gi = 0; gi < NGL; ++gi) {
+          const int hd = NG == 4 ? c : 2 * c + gi;  // the lane's head(s)
+          float v = sg[0];
+#pragma unroll
+          for (int g = 1; g < NG; ++g) v = hd == g ? sg[g] : v;
+          s[gi] = v;
+        }
+        bool grow = false;
+#pragma unroll
+        for (int gi = 0; gi < NGL; ++gi) grow = grow || s[gi] > m_run[gi] + kLazyLog2;
+        if (__any_sync(kFull, grow)) {
+          float alpha[NGL];
+#pragma unroll
+          for (int gi = 0; gi < NGL; ++gi) {
+            const float mnew = fmaxf(m_run[gi], s[gi]);
+            alpha[gi] = mnew == -INFINITY ? 1.f : fast_exp2(m_run[gi] - mnew);
+            l_run[gi] *= alpha[gi];
+            m_run[gi] = mnew;
+          }
+          if constexpr (NG == 4) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) O[q][jj] *= alpha[0];
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              O[q][0] *= alpha[0]; O[q][2] *= alpha[0];
+              O[q][1] *= alpha[NGL - 1]; O[q][3] *= alpha[NGL - 1];
+            }
           }
         }
-      }
+        float pr[NGL];
 #pragma unroll
-      for (int g = 0; g < NG; ++g) {
-        if (g >= G) break;
-        reinterpret_cast<float4*>(merge + (warp * G + g) * kHeadDim)[lane] =
-            make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
-        if (lane == 0) mlbuf[warp * G + g] = make_float2(mr[g], lr[g]);
-      }
-      consumer_sync<NW>();
-      for (int i = tid; i < G * (kHeadDim / 4); i += kConsumerThreads) {
-        const int g = i / (kHeadDim / 4), d4 = i % (kHeadDim / 4);
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, mlbuf[w * G + g].x);
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        float l = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int w = 0; w < NW; ++w) {
-            const float2 ml = mlbuf[w * G + g];
-            const float f = fast_exp2(ml.x - M);
-            const float4 v = reinterpret_cast<const float4*>(merge + (w * G + g) * kHeadDim)[d4];
-            o.x = fmaf(f, v.x, o.x);
-            o.y = fmaf(f, v.y, o.y);
-            o.z = fmaf(f, v.z, o.z);
-            o.w = fmaf(f, v.w, o.w);
-            l = fmaf(f, ml.y, l);
-          }
+        for (int gi = 0; gi < NGL; ++gi) {
+          pr[gi] = fast_exp2(s[gi] - (m_run[gi] == -INFINITY ? 0.f : m_run[gi]));
+          if (r == 0) l_run[gi] += pr[gi];  // the warp's sum adds the 8 lanes of a head once
         }
-        const long long row = static_cast<long long>(u.b) * p.hq + u.kvh * G + g;
-        pdl_wait();  // no-op: this kernel is the first of its call
-        reinterpret_cast<float4*>(p.res_o + row * kHeadDim)[d4] = o;
-        if (d4 == 0) p.res_ml[row] = make_float2(M, l);
+        // value elements 16 r .. 16 r + 15: the lane's output rows
+        const uint4 w0 = reinterpret_cast<const uint4*>(vr + 32 * r)[0];
+        const uint4 w1 = reinterpret_cast<const uint4*>(vr + 32 * r)[1];
+        float vf[4][4];
+        unpack(make_uint2(w0.x, w0.y), vf[0]);
+        unpack(make_uint2(w0.z, w0.w), vf[1]);
+        unpack(make_uint2(w1.x, w1.y), vf[2]);
+        unpack(make_uint2(w1.z, w1.w), vf[3]);
+        if constexpr (NG == 4) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) O[q][jj] = fmaf(pr[0], vf[q][jj], O[q][jj]);
+        } else {
+          // head 2c + gi: element 16r + 4i + {0, 1, 2, 3} sits in O[2i][gi],
+          // O[2i][2 + gi], O[2i + 1][gi], O[2i + 1][2 + gi]
+#pragma unroll
+          for (int i4 = 0; i4 < 4; ++i4)
+#pragma unroll
+            for (int gi = 0; gi < NGL; ++gi) {
+              O[2 * i4][gi] = fmaf(pr[gi], vf[i4][0], O[2 * i4][gi]);
+              O[2 * i4][2 + gi] = fmaf(pr[gi], vf[i4][1], O[2 * i4][2 + gi]);
+              O[2 * i4 + 1][gi] = fmaf(pr[gi], vf[i4][2], O[2 * i4 + 1][gi]);
+              O[2 * i4 + 1][2 + gi] = fmaf(pr[gi], vf[i4][3], O[2 * i4 + 1][2 + gi]);
+            }
+        }
+      };
+      // chunks of T tokens; the first was copied at unit start
+      for (int c0 = 0; c0 < n; c0 += T) {
+        if (c0 > 0) {
+          consumer_sync<NW>();  // every warp is done with the previous chunk
+          res_issue(u, t0 + c0, min(n - c0, T), false);
+          asm volatile("cp.async.wait_all;" ::: "memory");
+          consumer_sync<NW>();
+        }
+        for (int i = warp; i < min(n - c0, T); i += NW) token(rs + i * 256, rs + T * 256 + i * 256);
       }
-      consumer_sync<NW>();  // the merge buffer is free for the unit's own merge
     }
   };
 
@@ -1365,8 +1405,19 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   for (int k = 0; k < n_units; ++k) {
     const UnitStages u = unit_stages<kStageTok>(p, k, clamp_len(ulen_c[k]));
     if (k > 0) consumer_sync<NW>();  // previous unit's merge buffers and q~ are free
+    // Full-precision residual window (VecInfer, 实验结果 / 实验设置: the most
+    // recent tokens stay unquantized): the unit of split s takes window
+    // tokens [s R / S, (s + 1) R / S) of its (sequence, KV head) and merges
+    // them into its own online softmax after its stages, with s = q . k *
+    // scale * log2(e) from the raw query and key (the log2 domain of q~'s
+    // scores).  The slice's first res_tok rows and the raw queries are copied
+    // to shared memory with cp.async here, while the stages stream.
+    int res_t0 = 0, res_n = 0;
     if constexpr (kResidual) {
-      if (u.s == p.splits - 1) residual_partial(u);
+      const int R = ures_c[k];
+      res_t0 = u.s * R / p.splits;
+      res_n = (u.s + 1) * R / p.splits - res_t0;
+      res_issue(u, res_t0, min(res_n, p.res_tok), true);
     }
     if (k > 0) {
       transform_query(k);
@@ -1479,6 +1530,10 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       float sc[4];
       if constexpr (kLut) fused_lut(sc, false);
       else fused(sc, false);
+    }
+    if constexpr (kResidual) {
+      residual_merge(res_t0, res_n, u);
+      consumer_sync<NW>();  // the window slice (in the merge buffer) has been read
     }
 
     // ---- merge the consumer warps of this unit, write the split partial ------

@@ -68,15 +68,14 @@ struct DecodeParams {
   uint8_t* k_pool_w;          // the pools, written (k_pool / v_pool as writable pointers)
   uint8_t* v_pool_w;
   // Full-precision residual window inside the attention kernel (residual != 0):
-  // the unit of each (sequence, KV head)'s last split turns the window's
-  // tokens into one more partial (res_o, res_ml), merged by the combine.
+  // the unit of split s of each (sequence, KV head) merges window tokens
+  // [s R / S, (s + 1) R / S) into its own partial.
   int residual;
   const void* k_res;          // fp16 [B][Hkv][res_capacity][128]
   const void* v_res;
   const int32_t* res_lens;    // [B], clamped to [0, res_capacity]
   int res_capacity;
-  float* res_o;               // fp32 [B * Hq][128]
-  float2* res_ml;             // [B * Hq]: (m, l), log2 domain
+  int res_tok;                // window tokens staged in shared memory at a time
   float res_scale_log2;       // softmax scale * log2(e) (raw q . k)
 };
 
@@ -99,8 +98,6 @@ struct DequantParams {
 struct CombineParams {
   const float* ws_o;
   const float2* ws_ml;
-  const float* res_o;         // optional residual partials [B * Hq][128] (NULL: none)
-  const float2* res_ml;       // [B * Hq], merged as split number `splits`
   void* out;                  // fp16 [B][Hq][128]
   int rows;                   // B * Hq
   int splits;
@@ -111,6 +108,7 @@ constexpr int kProducerWarps = 4;  // TMA-issuing warps (one in four stages each
 constexpr int kMaxUnitsPerCta = 256;
 constexpr int kUnitTok = 32;       // split boundaries are multiples of this many tokens
 
+constexpr int kMaxResTok = 64;     // residual window tokens staged in shared memory at a time, at most
 constexpr int kMaxStages = 16;     // pipeline slots of the split kernel, at most
 
 // Consumer shape: `warps` consumer warps, each taking one 16-token mma chunk
@@ -165,22 +163,25 @@ __host__ __device__ inline int append_enc_bytes(int k_bits, int v_bits, int k_su
 // method's fp32 V codebook after them.
 __host__ __device__ inline DecodeSmem decode_smem(int k_bits, int v_bits, int group, int k_row,
                                                   int v_row, int nstage, int warps, int stage_tok,
-                                                  int append_enc = 0, int method = 0, int residual = 0) {
+                                                  int append_enc = 0, int method = 0, int res_tok = 0) {
   DecodeSmem s;
   int o = 0;
   const int rows = 1 << (k_bits > v_bits ? k_bits : v_bits);
   s.tab = o; o = align128(o + rows * (k_bits == 12 ? kTabRowWide : method ? kTabRow / 2 : kTabRow));
   s.qt = o; o = align128(o + (group > 4 ? 8 : 4) * 128 * 4);  // q~ operand table, 4 or 8 heads
+  // the merge buffer also holds a unit's residual window tokens (res_tok of
+  // them at a time: K and V rows, then the raw queries)
   const int merge = method ? 0 : warps * group * 128 * 4;
-  s.merge = o; o = align128(o + merge);
+  const int res = res_tok ? 2 * res_tok * 256 + 8 * 256 : 0;
+  s.merge = o; o = align128(o + (merge > res ? merge : res));
   s.ml = o; o = align128(o + warps * (group > 4 ? 8 : 4) * 8);
-  s.units = o; o = align128(o + 2 * kMaxUnitsPerCta * 4);  // consumer and producer copies
+  s.units = o; o = align128(o + 3 * kMaxUnitsPerCta * 4);  // lengths (consumers, producers), window lengths
   s.meta = o; o = align128(o + nstage * 16);
   s.bar = o; o = align128(o + (nstage * 2 + 1) * 8);  // full and empty per slot, then the append's
   s.flag = o; o = align128(o + 16);
   s.enc = o; o = align128(o + append_enc);
   s.aux = o; o = align128(o + (method ? kLutBytes : 0) + (method == 2 ? (1 << v_bits) * 4 * 4 : 0));
-  s.res = o; (void)residual;  // the residual window uses the merge buffer
+  s.res = s.merge;
   s.stage = o; o = align128(o + nstage * stage_tok * (k_row + v_row));
   s.total = o;
   return s;

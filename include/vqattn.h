@@ -342,11 +342,14 @@ vq_status vq_decode_step(const vq_layout* layout, int32_t batch, const void* q, 
  *   res_lens      int32 [batch], clamped to [0, res_capacity].
  *   res_capacity  1 .. 4096.
  *   workspace     at least vq_decode_residual_workspace_bytes(layout, batch,
- *                 max_seq_len, num_splits, 0) bytes, 256-byte aligned.
+ *                 max_seq_len, num_splits, 0) bytes (the same as
+ *                 vq_decode_workspace_bytes: the window joins the split
+ *                 partials), 256-byte aligned; no initialisation needed.
  * Two kernels on `stream`: the split attention over the codes, in which the
- * work unit of each (sequence, KV head)'s last split also turns the window's
- * tokens into one more partial, and the merge, which takes that partial as
- * one more split.  Moving tokens from the residual into
+ * work unit of split s of each (sequence, KV head) also merges window tokens
+ * [s R / S, (s + 1) R / S) (R = res_lens[b], S splits) into its own partial
+ * with the same online softmax, and the merge of the splits.  Moving tokens
+ * from the residual into
  * the cache (vq_encode_kv) is the caller's policy.  Other arguments and errors
  * as in vq_decode_attention.  A sequence with no token at all gives a zero
  * row.

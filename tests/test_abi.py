@@ -129,12 +129,12 @@ def test_check_layout_one_and_a_half_bit(lib):
         assert e.value.status == vq.VQ_ERR_UNSUPPORTED, kw
 
 
-def test_residual_workspace_is_the_split_workspace_plus_one_partial_per_row(lib):
+def test_residual_workspace_is_the_split_workspace(lib):
+    # the window's tokens join the split partials: no extra partial per row
     L = vq.make_layout()
     n = vq.vq_decode_workspace_bytes(L, 3, 32769, 19, 152)
     r = vq.vq_decode_residual_workspace_bytes(L, 3, 32769, 19, 152)
-    rows = 3 * 32
-    assert r == n + (rows * 128 * 4 + 255) // 256 * 256 + (rows * 8 + 255) // 256 * 256
+    assert r == n
     assert vq.vq_decode_residual_workspace_bytes(L, 3, 32769, 0, 152) == \
         vq.vq_decode_residual_workspace_bytes(L, 3, 32769, vq.vq_default_num_splits(L, 3, 32769, 152), 152)
     assert vq.vq_decode_residual_workspace_bytes(L, -1, 10, 0, 152) == 0

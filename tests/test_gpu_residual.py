@@ -102,6 +102,20 @@ def test_residual_default_splits_and_short_capacity():
         check_outputs(got[b, rows], ref, f"seq {b}")
 
 
+def test_residual_window_in_several_chunks():
+    # one split: a unit's window slice is the whole window, staged in shared
+    # memory 64 tokens at a time (five chunks for 300 tokens, edges 64 / 65)
+    w = W.custom(name="res-chunks", batch=3, num_q_heads=8, num_kv_heads=2, context=900, k_sub=4,
+                 v_sub=4, page_size=32, ragged=True, ragged_lo=400, ragged_hi=900, permuted_pages=True)
+    case = ResidualCase(w, calib_for(w), [300, 65, 64], 300)
+    q = W.queries(w)
+    got = case.run(q, num_splits=1)
+    assert case.gc.device_status() == 0
+    for b in range(w.batch):
+        ref, rows = case.oracle(q, b)
+        check_outputs(got[b, rows], ref, f"seq {b} residual {case.res_lens[b]}")
+
+
 def test_residual_zero_equals_decode_attention():
     w = _workload((2, 8, 4, 9), 5)
     case = ResidualCase(w, calib_for(w), [0, 0, 0], 64)
