@@ -95,16 +95,25 @@ int pick_splits(const vq_layout& L, int batch, int max_seq_len, int sms) {
   return best;
 }
 
+// Codebooks of 1024 centroids or more: the decode step's append is spread
+// over kAppendSlices CTAs per vector.
+bool sliced_append(const vq_layout& L) { return L.k_bits >= 10 || L.v_bits >= 10; }
+
 struct WsLayout {
-  size_t o_off, ml_off, total;
+  size_t o_off, ml_off, cand_off, total;
 };
 
+// Split partials, then (large codebooks) the sliced append's candidates.
 WsLayout ws_layout(const vq_layout& L, int batch, int splits) {
   WsLayout w;
   const size_t rows = static_cast<size_t>(batch) * L.num_q_heads * splits;
   w.o_off = 0;
   w.ml_off = (rows * L.head_dim * sizeof(float) + 255) & ~size_t(255);
-  w.total = w.ml_off + ((rows * 2 * sizeof(float) + 255) & ~size_t(255));
+  w.cand_off = w.ml_off + ((rows * 2 * sizeof(float) + 255) & ~size_t(255));
+  const size_t cand = sliced_append(L) ? static_cast<size_t>(batch) * L.num_kv_heads * 2 *
+                                             vqk::kAppendSlices * 32 * 4 * sizeof(int2)
+                                       : 0;
+  w.total = w.cand_off + cand;
   return w;
 }
 
@@ -154,7 +163,7 @@ vq_status vq_check_layout(const vq_layout* layout, int32_t for_decode) {
 // shape follows from the number of vectors.
 vq_status launch_encode_impl(const vq_layout& L, vqk::EncodeParams& p, int32_t num_tokens,
                              bool has_k, bool has_v, void* stream, const char* what,
-                             bool overlap) {
+                             bool overlap, int2* cand = nullptr) {
   p.sub[0] = L.k_sub;
   p.sub[1] = L.v_sub;
   p.bits[0] = L.k_bits;
@@ -172,7 +181,10 @@ vq_status launch_encode_impl(const vq_layout& L, vqk::EncodeParams& p, int32_t n
   const bool multi_ok = (!has_k || L.k_sub == 2 || L.k_sub == 4) && (!has_v || L.v_sub == 2 || L.v_sub == 4);
   p.vec_per_warp = (p.split == 1 && multi_ok) ? vqk::kMultiVec : 1;
   const int per_cta = 8 * p.vec_per_warp / p.split;
-  const long long grid_x = (vectors + per_cta - 1) / per_cta;
+  // a few vectors of a large codebook (with candidate space): several CTAs each
+  p.slices = (cand && p.split > 1 && sliced_append(L)) ? vqk::kAppendSlices : 1;
+  p.cand = cand;
+  const long long grid_x = (vectors + per_cta - 1) / per_cta * p.slices;
   if (grid_x > 0x7fffffffLL) return fail(VQ_ERR_INVALID_ARG, "too many tokens (%d)", num_tokens);
   p.which_base = has_k ? 0 : 1;
   const int grid_y = (has_k && has_v) ? 2 : 1;
@@ -185,6 +197,10 @@ vq_status launch_encode_impl(const vq_layout& L, vqk::EncodeParams& p, int32_t n
   cudaError_t e = vqk::launch_encode(p, static_cast<int>(grid_x), grid_y, smem,
                                      static_cast<cudaStream_t>(stream), overlap);
   if (e != cudaSuccess) return cuda_fail(e, what);
+  if (p.slices > 1) {
+    e = vqk::launch_encode_merge(p, static_cast<int>(vectors), grid_y, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, what);
+  }
   return VQ_OK;
 }
 
@@ -597,7 +613,12 @@ vq_status vq_decode_step(const vq_layout* layout, int32_t batch, const void* q, 
   ep.max_pages = max_pages_per_seq;
   ep.status = status;
   ep.num_slots = static_cast<long long>(num_pages) * L.page_size;
-  st = launch_encode_impl(L, ep, batch, true, true, stream, "vq_decode_step append encode", false);
+  // a large codebook's append goes over several CTAs per vector, its
+  // candidates in the workspace after the split partials
+  const WsLayout wsl = ws_layout(L, batch, p.splits);
+  int2* cand = sliced_append(L) ? reinterpret_cast<int2*>(static_cast<uint8_t*>(workspace) + wsl.cand_off)
+                                : nullptr;
+  st = launch_encode_impl(L, ep, batch, true, true, stream, "vq_decode_step append encode", false, cand);
   if (st != VQ_OK) return st;
   // 2. split attention (its copies wait for the append), 3. merge of the splits
   st = launch_partial(L, p, grid, smem, stream, true);

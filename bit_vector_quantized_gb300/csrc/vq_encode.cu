@@ -19,7 +19,10 @@
 // Many vectors with d = 2 or 4 (a prefill) go four to a warp, sharing every
 // centroid load.  With few tokens (a decode-step append) the scan of one
 // vector is split over `split` warps that each take a slice of the codebook,
-// and the slices are merged keeping the lowest index on ties.
+// and the slices are merged keeping the lowest index on ties.  A large
+// codebook (the 1.5-bit format's 4096 centroids of 8) is also split over
+// several CTAs per vector, each preparing and scanning its own part of the
+// table; a one-warp merge kernel combines their candidates in order.
 // Finally the warp packs the codes into the LSB-first bit stream of the row
 // (one 32-bit word per lane) and stores it into the token's paged slot.
 #include "vq_device.cuh"
@@ -188,7 +191,8 @@ struct VecIn {
 __device__ __forceinline__ VecIn load_vector(const EncodeParams& p, int which) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int group = warp / p.split;
-  const long long th = static_cast<long long>(blockIdx.x) * (kEncWarps / p.split) + group;
+  const long long bx = p.slices > 1 ? blockIdx.x / p.slices : blockIdx.x;
+  const long long th = bx * (kEncWarps / p.split) + group;
   VecIn in;
   in.active = th < static_cast<long long>(p.num_tokens) * p.hkv;
   in.t = in.active ? th / p.hkv : 0;
@@ -263,14 +267,12 @@ __device__ __forceinline__ void pack_store(const EncodeParams& p, int which, con
 
 template <int D>
 __device__ void encode_vector(const EncodeParams& p, int which, const VecIn& in, const float* cmul,
-                              const float* cnorm, float* red_best, int* red_idx) {
+                              const float* cnorm, float* red_best, int* red_idx, int cs0, int cs1) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = p.split;
   const int wing = warp % split;
   const bool active = in.active;
   const int h = in.h;
-  const int bits = p.bits[which];
-  const int ncent = 1 << bits;
 
   float x[4];
   {
@@ -292,8 +294,9 @@ __device__ void encode_vector(const EncodeParams& p, int which, const VecIn& in,
     for (int e = 0; e < 4; ++e) x[e] *= r;
   }
 
-  const int j0 = static_cast<int>((static_cast<long long>(wing) * ncent) / split);
-  const int j1 = static_cast<int>((static_cast<long long>(wing + 1) * ncent) / split);
+  // the warp's slice of the CTA's centroids [cs0, cs1)
+  const int j0 = cs0 + static_cast<int>((static_cast<long long>(wing) * (cs1 - cs0)) / split);
+  const int j1 = cs0 + static_cast<int>((static_cast<long long>(wing + 1) * (cs1 - cs0)) / split);
   float best[4];
   int idx[4];
   scan_centroids<D>(x, cmul, cnorm, j0, j1, lane, best, idx);
@@ -318,8 +321,54 @@ __device__ void encode_vector(const EncodeParams& p, int which, const VecIn& in,
     }
   }
   if (wing != 0) return;
-
+  if (p.slices > 1) {  // this CTA's candidates; the merge kernel stores the row
+    if (!active) return;
+    const long long v = in.t * p.hkv + h;
+    int2* c = p.cand + ((v * 2 + which) * p.slices + blockIdx.x % p.slices) * 32 * 4 + lane * 4;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) c[s] = make_int2(__float_as_int(best[s]), idx[s]);
+    return;
+  }
   pack_store<D>(p, which, idx, active, h, in.slot);
+}
+
+// Merge of a sliced append (slices > 1): the warp of (vector, tensor) reads the
+// slices' candidates in slice order, which cover increasing index ranges, so a
+// strict '<' keeps the lowest index among equal scores, then packs and stores
+// the row.
+__global__ void __launch_bounds__(32) vq_encode_merge_kernel(const EncodeParams p) {
+  const int lane = threadIdx.x;
+  const long long v = blockIdx.x;
+  const int which = blockIdx.y + p.which_base;
+  pdl_trigger();
+  const long long t = v / p.hkv;
+  const int h = static_cast<int>(v % p.hkv);
+  const long long slot = token_slot(p, t);
+  pdl_wait();  // the candidates are written by the previous kernel
+  float best[4];
+  int idx[4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    best[s] = INFINITY;
+    idx[s] = 0x7fffffff;
+  }
+  const int2* c = p.cand + (v * 2 + which) * p.slices * 32 * 4 + lane * 4;
+  for (int sl = 0; sl < p.slices; ++sl) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int2 e = __ldcg(c + sl * 32 * 4 + s);
+      if (__int_as_float(e.x) < best[s]) {
+        best[s] = __int_as_float(e.x);
+        idx[s] = e.y;
+      }
+    }
+  }
+  switch (p.sub[which]) {
+    case 1: pack_store<1>(p, which, idx, true, h, slot); break;
+    case 2: pack_store<2>(p, which, idx, true, h, slot); break;
+    case 4: pack_store<4>(p, which, idx, true, h, slot); break;
+    default: pack_store<8>(p, which, idx, true, h, slot); break;
+  }
 }
 
 // Cache fill of many vectors (prefill): each warp encodes NV consecutive
@@ -453,18 +502,22 @@ __global__ void __launch_bounds__(kEncWarps * 32) vq_encode_kernel(const EncodeP
   // the codebook table: each thread loads four centroids (one vector load
   // each) before it uses any, so a large codebook costs a few L2 round trips
   const __half* cb = static_cast<const __half*>(p.cb[which]);
+  // the CTA's centroids: all of them, or its slice of a sliced append
+  const int sl = p.slices > 1 ? static_cast<int>(blockIdx.x % p.slices) : 0;
+  const int cs0 = p.slices > 1 ? static_cast<int>((static_cast<long long>(sl) * ncent) / p.slices) : 0;
+  const int cs1 = p.slices > 1 ? static_cast<int>((static_cast<long long>(sl + 1) * ncent) / p.slices) : ncent;
   constexpr int kPrepBatch = 4;
-  for (int j0 = threadIdx.x; j0 < ncent; j0 += kPrepBatch * blockDim.x) {
+  for (int j0 = cs0 + static_cast<int>(threadIdx.x); j0 < cs1; j0 += kPrepBatch * blockDim.x) {
     __half c[kPrepBatch][8];
 #pragma unroll
     for (int u = 0; u < kPrepBatch; ++u) {
       const int j = j0 + u * static_cast<int>(blockDim.x);
-      if (j < ncent) load_centroid(cb, j, d, c[u]);
+      if (j < cs1) load_centroid(cb, j, d, c[u]);
     }
 #pragma unroll
     for (int u = 0; u < kPrepBatch; ++u) {
       const int j = j0 + u * static_cast<int>(blockDim.x);
-      if (j >= ncent) break;
+      if (j >= cs1) break;
       float n = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -483,10 +536,10 @@ __global__ void __launch_bounds__(kEncWarps * 32) vq_encode_kernel(const EncodeP
   }
   __syncthreads();
   switch (d) {
-    case 1: encode_vector<1>(p, which, in, cmul, cnorm, red_best, red_idx); break;
-    case 2: encode_vector<2>(p, which, in, cmul, cnorm, red_best, red_idx); break;
-    case 4: encode_vector<4>(p, which, in, cmul, cnorm, red_best, red_idx); break;
-    default: encode_vector<8>(p, which, in, cmul, cnorm, red_best, red_idx); break;
+    case 1: encode_vector<1>(p, which, in, cmul, cnorm, red_best, red_idx, cs0, cs1); break;
+    case 2: encode_vector<2>(p, which, in, cmul, cnorm, red_best, red_idx, cs0, cs1); break;
+    case 4: encode_vector<4>(p, which, in, cmul, cnorm, red_best, red_idx, cs0, cs1); break;
+    default: encode_vector<8>(p, which, in, cmul, cnorm, red_best, red_idx, cs0, cs1); break;
   }
 }
 
@@ -503,6 +556,12 @@ cudaError_t launch_encode(const EncodeParams& p, int grid_x, int grid_y, size_t 
   cudaError_t e = ensure_smem(vq_encode_kernel, smem, opt_in);
   if (e != cudaSuccess) return e;
   e = launch_pdl(vq_encode_kernel, dim3(grid_x, grid_y), dim3(kEncWarps * 32), smem, stream, p, overlap);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_encode_merge(const EncodeParams& p, int vectors, int grid_y, cudaStream_t stream) {
+  if (vectors == 0) return cudaSuccess;
+  cudaError_t e = launch_pdl(vq_encode_merge_kernel, dim3(vectors, grid_y), dim3(32), 0, stream, p, true);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -27,6 +27,12 @@ struct EncodeParams {
   int split;             // warps per token-head: 1, 2, 4 or 8
   int which_base;        // blockIdx.y + which_base selects keys (0) or values (1)
   int vec_per_warp;      // 1, or kMultiVec (prefill with sub-vector lengths 2 / 4; split == 1)
+  // A decode-step append with a large codebook can be spread over `slices`
+  // CTAs per vector: CTA c scans centroids [c N / slices, (c + 1) N / slices)
+  // and leaves its argmin candidates in `cand`; the merge kernel then merges
+  // the slices in order (lowest index on ties) and stores the row.
+  int slices;            // 1: each CTA stores its vectors' rows itself
+  int2* cand;            // [vectors][2 tensors][slices][32 lanes][4] (score bits, index)
   // Decode-step append (slots == NULL): token t is the new token of sequence t,
   // stored at position seq_lens[t] - 1 through the page table.
   const int32_t* page_table;  // [T][max_pages]
@@ -244,6 +250,9 @@ inline cudaError_t ensure_smem(K kern, size_t smem, SmemOptIn& st) {
 cudaError_t launch_encode(const EncodeParams& p, int grid_x, int grid_y, size_t smem,
                           cudaStream_t stream, bool overlap);
 size_t encode_smem_bytes(int sub, int bits);
+// The merge of a sliced append's candidates: one warp per (vector, tensor).
+cudaError_t launch_encode_merge(const EncodeParams& p, int vectors, int grid_y, cudaStream_t stream);
+constexpr int kAppendSlices = 8;  // CTAs per vector for appends with 1024 or more centroids
 
 // Returns cudaErrorInvalidValue when no kernel is compiled for the formats.
 cudaError_t launch_decode(const DecodeParams& p, int k_sub, int k_bits, int v_sub, int v_bits,

@@ -173,9 +173,12 @@ vq_status vq_dequantize_kv(const vq_layout* layout, int32_t num_tokens,
                            int32_t* status, void* stream);
 
 /*
- * Workspace bytes vq_decode_attention needs for `batch` sequences split
- * `num_splits` ways (num_splits <= 0: the value vq_default_num_splits picks).
- * Pure host arithmetic.  Returns 0 for invalid arguments.
+ * Workspace bytes vq_decode_attention (and vq_decode_step) needs for `batch`
+ * sequences split `num_splits` ways (num_splits <= 0: the value
+ * vq_default_num_splits picks): the split partials, and for codebooks of 1024
+ * centroids or more (10- to 12-bit codes) also the candidates of
+ * vq_decode_step's append, which spreads each new vector's codebook scan over
+ * several CTAs.  Pure host arithmetic.  Returns 0 for invalid arguments.
  */
 size_t vq_decode_workspace_bytes(const vq_layout* layout, int32_t batch,
                                  int32_t max_seq_len, int32_t num_splits, int32_t num_sms);
@@ -304,7 +307,10 @@ vq_status vq_decode_partial_method(const vq_layout* layout, int32_t batch, const
  *     向量量化KV缓存, where the new code joins the cached ones);
  *   - otherwise three kernels: the append encode, the split attention (it
  *     starts while the append runs, prepares its tables, and waits for the
- *     append before it reads the pools) and the merge.
+ *     append before it reads the pools) and the merge; with 10- to 12-bit
+ *     codes the append is two kernels (each new vector's codebook scan split
+ *     over several CTAs whose candidates sit in the workspace, then their
+ *     merge and the store).
  *   k_new, v_new fp16 [batch][Hkv][D]: the new token of every sequence.  It is
  *                token seq_lens[b] - 1 of sequence b and goes to slot
  *                page_table[b][t / P] * P + t % P of the pools
