@@ -129,6 +129,16 @@ def test_check_layout_one_and_a_half_bit(lib):
         assert e.value.status == vq.VQ_ERR_UNSUPPORTED, kw
 
 
+def test_workspace_holds_the_sliced_append_candidates_for_large_codebooks(lib):
+    # 12-bit codebooks: the decode step's append leaves 8 slices x 32 lanes x 4
+    # (score, index) candidates per new vector and tensor after the partials
+    small = vq.make_layout()
+    wide = vq.make_layout(k_sub=8, k_bits=12, v_sub=8, v_bits=12)
+    n = vq.vq_decode_workspace_bytes(small, 3, 32769, 19, 152)
+    w = vq.vq_decode_workspace_bytes(wide, 3, 32769, 19, 152)
+    assert w == n + 3 * 8 * 2 * 8 * 32 * 4 * 8
+
+
 def test_residual_workspace_is_the_split_workspace(lib):
     # the window's tokens join the split partials: no extra partial per row
     L = vq.make_layout()
