@@ -152,3 +152,49 @@ def test_step_length_beyond_max_seq_len():
     assert a.device_status() == 0 and b.device_status() == 0
     assert torch.equal(a.k_pool, b.k_pool) and torch.equal(a.v_pool, b.v_pool)
     assert torch.equal(got, ref)
+
+
+def test_step_replayed_from_a_cuda_graph():
+    # replays of one captured call, over a workspace holding stale bytes, must
+    # all give the separate calls' output (the append inside the attention
+    # kernel, then the merge of the splits)
+    w = _workload((4, 8, 4, 8), 4, batch=3, context=700)
+    _, a, b = _pair(w)
+    q = W.queries(w)
+    a.append()
+    ref = a.decode(q, num_splits=5)
+    vq, dev = b.vq, b.device
+    lens = b.lens + 1
+    pos = [int(n) - 1 for n in lens]
+    k = np.stack([W.kv_tokens(w, bb, "k", p, p + 1)[0] for bb, p in enumerate(pos)])
+    v = np.stack([W.kv_tokens(w, bb, "v", p, p + 1)[0] for bb, p in enumerate(pos)])
+    q_d, k_d, v_d = (torch.from_numpy(x).to(dev) for x in (q, k, v))
+    seq = torch.from_numpy(lens.astype(np.int32)).to(dev)
+    ml = int(lens.max())
+    wsb = vq.vq_decode_workspace_bytes(b.layout, w.batch, ml, 5)
+    ws = torch.full((wsb,), 0xA5, dtype=torch.uint8, device=dev)  # stale bytes
+    out = torch.empty((w.batch, w.num_q_heads, 128), dtype=torch.float16, device=dev)
+    P = lambda t: t.data_ptr()  # noqa: E731
+
+    def call():
+        vq.vq_decode_step(b.layout, w.batch, P(q_d), P(k_d), P(v_d), P(b.lam), P(b.ck), P(b.cv),
+                          P(b.k_pool), P(b.v_pool), b.num_pages, P(b.page_table),
+                          b.page_table.shape[1], P(seq), ml, 0.0, 5, P(out), P(ws), wsb,
+                          P(b.status), torch.cuda.current_stream().cuda_stream)
+
+    call()
+    torch.cuda.synchronize()
+    assert np.array_equal(out.float().cpu().numpy(), ref)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            call()
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(out.float().cpu().numpy(), ref)
+    assert b.device_status() == 0
