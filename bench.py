@@ -89,6 +89,17 @@ def load_calib(i):
     return z["lam"], z["ck"], z["cv"]
 
 
+def step_launches(w, sms):
+    """Kernels one vq_decode_step launches (include/vqattn.h): two when the
+    attention kernel appends itself (codes of at most 9 bits, at most one
+    sequence-KV-head pair per SM), else the append encode, the attention kernel
+    and the merge, with one more (the candidates' merge) for 10- to 12-bit
+    codebooks."""
+    if w.k_bits <= 9 and w.v_bits <= 9 and w.batch * w.num_kv_heads <= sms:
+        return 2
+    return 4 if max(w.k_bits, w.v_bits) >= 10 else 3
+
+
 def tokens_per_step(w):
     return int((W.seq_lens(w) + 1).sum())
 
@@ -971,7 +982,8 @@ def main():
             "residual_window": residual,
             "other_workloads": others,
             "methods": methods,
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * K, "clocks": clocks,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": step_launches(w, sms) * K,
+            "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
