@@ -90,14 +90,19 @@ def load_calib(i):
 
 
 def step_launches(w, sms):
-    """Kernels one vq_decode_step launches (include/vqattn.h): two when the
-    attention kernel appends itself (codes of at most 9 bits, at most one
-    sequence-KV-head pair per SM), else the append encode, the attention kernel
-    and the merge, with one more (the candidates' merge) for 10- to 12-bit
-    codebooks."""
-    if w.k_bits <= 9 and w.v_bits <= 9 and w.batch * w.num_kv_heads <= sms:
-        return 2
-    return 4 if max(w.k_bits, w.v_bits) >= 10 else 3
+    """Kernels one vq_decode_step launches (include/vqattn.h).  With at most
+    one sequence-KV-head pair per SM the attention kernel appends the new
+    tokens itself: two kernels (with the merge), or three for the 1.5-bit
+    format (its sliced codebook scan first).  Otherwise the append encode, the
+    attention kernel and the merge, with one more (the candidates' merge) for
+    10- to 12-bit codebooks."""
+    wide = max(w.k_bits, w.v_bits) >= 10
+    if w.batch * w.num_kv_heads <= sms:
+        if w.k_bits <= 9 and w.v_bits <= 9:
+            return 2
+        if w.k_sub == 8 and w.k_bits == 12 and w.v_sub == 8 and w.v_bits == 12:
+            return 3
+    return 4 if wide else 3
 
 
 def tokens_per_step(w):

@@ -163,7 +163,7 @@ vq_status vq_check_layout(const vq_layout* layout, int32_t for_decode) {
 // shape follows from the number of vectors.
 vq_status launch_encode_impl(const vq_layout& L, vqk::EncodeParams& p, int32_t num_tokens,
                              bool has_k, bool has_v, void* stream, const char* what,
-                             bool overlap, int2* cand = nullptr) {
+                             bool overlap, int2* cand = nullptr, bool merge_kernel = true) {
   p.sub[0] = L.k_sub;
   p.sub[1] = L.v_sub;
   p.bits[0] = L.k_bits;
@@ -197,7 +197,7 @@ vq_status launch_encode_impl(const vq_layout& L, vqk::EncodeParams& p, int32_t n
   cudaError_t e = vqk::launch_encode(p, static_cast<int>(grid_x), grid_y, smem,
                                      static_cast<cudaStream_t>(stream), overlap);
   if (e != cudaSuccess) return cuda_fail(e, what);
-  if (p.slices > 1) {
+  if (p.slices > 1 && merge_kernel) {
     e = vqk::launch_encode_merge(p, static_cast<int>(vectors), grid_y, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, what);
   }
@@ -396,7 +396,8 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
     for (; ns >= vqk::kProducerWarps; --ns) {
       bytes = vqk::decode_smem(L.k_bits, L.v_bits, p.group, p.k_row, p.v_row, ns, sh.warps,
                                sh.stage_tok(),
-                               with_append ? vqk::append_enc_bytes(L.k_bits, L.v_bits, L.k_sub, L.v_sub) : 0,
+                               with_append && !sliced_append(L)
+                                   ? vqk::append_enc_bytes(L.k_bits, L.v_bits, L.k_sub, L.v_sub) : 0,
                                method, res_tok)
                   .total;
       if (optin <= 0 || bytes <= static_cast<size_t>(optin)) return ns;
@@ -570,35 +571,24 @@ vq_status vq_decode_step(const vq_layout* layout, int32_t batch, const void* q, 
   vqk::DecodeParams p;
   int grid = 0;
   size_t smem = 0;
-  // Formats with byte-aligned K codes encode the new token inside the
-  // attention kernel (one launch, then the merge) when the attention kernel's
-  // shape leaves room for it; the 1.5-bit format appends with the encode
-  // kernel first.
-  // The producer warps of one CTA encode each appended token while their
-  // first copies are in flight, so the fusion pays off while there is about
-  // one append per CTA; with more, the separate encode kernel spreads them
-  // over the GPU sooner (measured: 32K, ragged batch-16 and 196K steps faster
-  // fused, the batch-64 step slower).
+  // With at most one (sequence, KV head) pair per SM the new tokens are
+  // appended inside the attention kernel: the producer warps of the CTA whose
+  // split holds a new token encode it while their first copies are in flight
+  // (codes of at most 9 bits), or merge the candidates that the encode
+  // kernel's sliced scan left in the workspace (the 1.5-bit format, whose
+  // 4096-centroid scan needs more than one CTA).  With more pairs than SMs the
+  // separate append kernel spreads the appends over the GPU sooner (measured:
+  // 32K, ragged batch-16 and 196K steps faster fused, batch 64 no faster).
   const int sms_now = device_sms();
-  bool fused = L.k_bits <= 9 && L.v_bits <= 9 &&
+  const bool wide = sliced_append(L);
+  const bool wide_ok = L.k_sub == 8 && L.k_bits == 12 && L.v_sub == 8 && L.v_bits == 12;
+  bool fused = ((L.k_bits <= 9 && L.v_bits <= 9) || wide_ok) &&
                static_cast<long long>(batch) * L.num_kv_heads <= (sms_now > 0 ? sms_now : 0);
   st = prepare_decode(layout, batch, q, lambda, codebook_k, codebook_v, k_pool, v_pool, num_pages,
                       page_table, max_pages_per_seq, seq_lens, max_seq_len, softmax_scale,
                       num_splits, workspace, workspace_bytes, status, p, grid, smem, &fused);
   if (st != VQ_OK) return st;
-  if (fused) {
-    p.append = 1;
-    p.k_new = k_new;
-    p.v_new = v_new;
-    p.k_pool_w = static_cast<uint8_t*>(k_pool);
-    p.v_pool_w = static_cast<uint8_t*>(v_pool);
-    st = launch_partial(L, p, grid, smem, stream, false);
-    if (st != VQ_OK) return st;
-    return combine_impl(layout, batch, max_seq_len, p.splits, workspace, workspace_bytes, out, stream,
-                        true);
-  }
 
-  // 1. append: token seq_lens[b] - 1 of every sequence, slot from the page table
   vqk::EncodeParams ep{};
   ep.src[0] = k_new;
   ep.src[1] = v_new;
@@ -616,8 +606,31 @@ vq_status vq_decode_step(const vq_layout* layout, int32_t batch, const void* q, 
   // a large codebook's append goes over several CTAs per vector, its
   // candidates in the workspace after the split partials
   const WsLayout wsl = ws_layout(L, batch, p.splits);
-  int2* cand = sliced_append(L) ? reinterpret_cast<int2*>(static_cast<uint8_t*>(workspace) + wsl.cand_off)
-                                : nullptr;
+  int2* cand = wide ? reinterpret_cast<int2*>(static_cast<uint8_t*>(workspace) + wsl.cand_off) : nullptr;
+
+  if (fused) {
+    p.append = 1;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_pool_w = static_cast<uint8_t*>(k_pool);
+    p.v_pool_w = static_cast<uint8_t*>(v_pool);
+    bool overlap = false;
+    if (wide) {  // the sliced scan first; the attention kernel merges its candidates
+      st = launch_encode_impl(L, ep, batch, true, true, stream, "vq_decode_step append scan", false, cand,
+                              false);
+      if (st != VQ_OK) return st;
+      if (ep.slices <= 1) return fail(VQ_ERR_UNSUPPORTED, "vq_decode_step: the append scan was not sliced");
+      p.app_cand = cand;
+      p.app_slices = ep.slices;
+      overlap = true;
+    }
+    st = launch_partial(L, p, grid, smem, stream, overlap);
+    if (st != VQ_OK) return st;
+    return combine_impl(layout, batch, max_seq_len, p.splits, workspace, workspace_bytes, out, stream,
+                        true);
+  }
+
+  // 1. append: token seq_lens[b] - 1 of every sequence, slot from the page table
   st = launch_encode_impl(L, ep, batch, true, true, stream, "vq_decode_step append encode", false, cand);
   if (st != VQ_OK) return st;
   // 2. split attention (its copies wait for the append), 3. merge of the splits

@@ -459,14 +459,13 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   uint8_t* const smem = g_smem;
   const int G = p.group;
   const int NS = p.nstage;
-  static_assert(!kAppend || !kWide, "the 1.5-bit format appends with the encode kernel");
   static_assert(kMethod == kMethodGather ||
                     (DK == 4 && BK == 8 && DV == 4 && BV == 8 && NG == 4 && NW == 12 && !kAppend),
                 "the table-based methods are built for d = 4, 8-bit codes, G <= 4");
   constexpr bool kLut = kMethod == kMethodLut, kBins = kMethod == kMethodBins;
   static_assert(!kResidual || (kMethod == kMethodGather && !kAppend), "the residual window runs alone");
   const DecodeSmem L = decode_smem(BK, BV, G, KROW, VROW, NS, NW, kStageTok,
-                                   kAppend ? append_enc_bytes(BK, BV, DK, DV) : 0, kMethod,
+                                   kAppend && !kWide ? append_enc_bytes(BK, BV, DK, DV) : 0, kMethod,
                                    kResidual ? p.res_tok : 0);
   float* qt = reinterpret_cast<float*>(smem + L.qt);
   // the LUT method's merge buffer shares the LUT (built again for every unit)
@@ -662,8 +661,49 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
     // (lowest index on ties), pack the K and V rows and store them into the
     // pools through the page table, fencing the stores for the copy engine.
     // The stage holding an attended new token is issued only after this.
+    // The 1.5-bit format's codebooks are too large to scan here: the encode
+    // kernel launched before this one scans each new vector over several CTAs
+    // and leaves their candidates (app_cand); warps 0 and 1 merge them in
+    // slice order (lowest index on ties), then pack and store the rows.
     auto encode_phase = [&]() {
-      if constexpr (kAppend) {
+      if constexpr (kAppend && kWide) {
+        asm volatile("bar.sync 4, %0;" ::"n"((NW + NP) * 32) : "memory");
+        for (int k = 0; k < n_units && pw < 2; ++k) {
+          const int raw = ulen_p[k];
+          const UnitId id = unit_id(p, k);
+          if (!append_owned(p, id.s, raw)) continue;
+          const int pos = raw - 1;
+          const int pi = pos / P;
+          const int pg = pi < p.max_pages ? __ldg(p.page_table + static_cast<long long>(id.b) * p.max_pages + pi) : -1;
+          // lane i < 16 takes sub-vector i, whose candidate the encode kernel's lane 2i holds
+          const long long v = static_cast<long long>(id.b) * p.hkv + id.kvh;
+          int idx[2] = {0, 0};
+          if (lane < 16) {
+            const int2* cand = p.app_cand + (v * 2 + pw) * p.app_slices * 32 * 4 + (2 * lane) * 4;
+            float best = INFINITY;
+            int bi = 0x7fffffff;
+            for (int sl = 0; sl < p.app_slices; ++sl) {
+              const int2 e = __ldcg(cand + sl * 32 * 4);
+              if (__int_as_float(e.x) < best) {
+                best = __int_as_float(e.x);
+                bi = e.y;
+              }
+            }
+            idx[0] = bi;
+          }
+          const uint32_t word = pack_row_word<1, BK>(idx, lane);  // codes 16 .. 31 fall past the row
+          const int rb = pw == 0 ? KROW : VROW;
+          const bool okp = pg >= 0 && pg < p.num_pages;
+          if (!okp && lane == 0 && pw == 0) report(p.status, kDevBadPage);
+          if (okp && lane < rb / 4) {
+            uint8_t* pool = pw == 0 ? p.k_pool_w : p.v_pool_w;
+            const long long r0 = (static_cast<long long>(pg) * p.hkv + id.kvh) * P + pos % P;
+            reinterpret_cast<uint32_t*>(pool + r0 * rb)[lane] = word;
+            fence_proxy_async_global();
+          }
+        }
+        producer_sync<NP>();  // every new row is stored and fenced before its stage is copied
+      } else if constexpr (kAppend) {
         asm volatile("bar.sync 4, %0;" ::"n"((NW + NP) * 32) : "memory");  // the consumers' table and norms
         constexpr int NSK = DK == 2 ? 2 : 1, NSV = DV == 2 ? 2 : 1;
         for (int k = 0; k < n_units; ++k) {
@@ -859,7 +899,7 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   // Fused append: ||c||^2 and -2 c of every centroid in fp32, computed as the
   // encode kernel computes them (the norm a chain of fused multiply-adds in
   // element order; -2 c exact).
-  if constexpr (kAppend) {
+  if constexpr (kAppend && !kWide) {
 #pragma unroll
     for (int i = 0; i < kNK; ++i) {
       const int j = tid + i * kConsumerThreads;
@@ -870,7 +910,10 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
       const int j = tid + i * kConsumerThreads;
       if (j < (1 << BV)) append_tables<DV>(cbv_r[i], j, enc_vn, enc_vm);
     }
-    // the table and the norms are what the producers' encode reads
+  }
+  if constexpr (kAppend) {
+    // the tables and the norms (none for the 1.5-bit format) are what the
+    // producers' encode reads
     asm volatile("bar.arrive 4, %0;" ::"n"((NW + NP) * 32) : "memory");
   }
   // q~ = q diag(lambda) H_D * scale * log2(e), split into fp16 hi + lo parts
@@ -1676,7 +1719,7 @@ cudaError_t launch_formats(const DecodeParams& p, int grid, size_t smem, cudaStr
     return cudaErrorInvalidValue;
   }
   if (p.append) {  // the decode step with the append inside: the default shapes only
-    if constexpr (BK <= 9 && BV <= 9) {
+    if constexpr ((BK <= 9 && BV <= 9) || (DK == 8 && BK == 12)) {
       if (p.warps == 12 && !wide) return launch_split<DK, BK, DV, BV, 4, 12, true>(p, grid, smem, stream, ov);
       if (p.warps == 8)
         return wide ? launch_split<DK, BK, DV, BV, 8, 8, true>(p, grid, smem, stream, ov)

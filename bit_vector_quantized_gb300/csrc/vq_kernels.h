@@ -73,6 +73,10 @@ struct DecodeParams {
   const void* v_new;
   uint8_t* k_pool_w;          // the pools, written (k_pool / v_pool as writable pointers)
   uint8_t* v_pool_w;
+  // the 1.5-bit format: the encode kernel's sliced-scan candidates
+  // [vectors][2 tensors][app_slices][32 lanes][4] (score bits, index)
+  const int2* app_cand;
+  int app_slices;
   // Full-precision residual window inside the attention kernel (residual != 0):
   // the unit of split s of each (sequence, KV head) merges window tokens
   // [s R / S, (s + 1) R / S) into its own partial.

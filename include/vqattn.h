@@ -297,14 +297,16 @@ vq_status vq_decode_partial_method(const vq_layout* layout, int32_t batch, const
  * vq_decode_attention with the same split count, without a slot mapping: the
  * slots come from the page table.  Two ways, chosen by the library and equal
  * bit for bit:
- *   - with at most one sequence-KV-head pair per SM and a format whose codes
- *     are at most 9 bits (every format but the 1.5-bit one), the attention
- *     kernel itself encodes each new token (the producer warps of the CTA
- *     whose split holds it encode it while their first copies are in flight
- *     and store the codes; the stage that holds the token is copied only
- *     after the store), then the merge: two kernels
- *     (the fused append of HACK's decode kernel and of VecInfer's 注意力机制中的
- *     向量量化KV缓存, where the new code joins the cached ones);
+ *   - with at most one sequence-KV-head pair per SM, the attention kernel
+ *     itself appends each new token (the producer warps of the CTA whose
+ *     split holds it encode it while their first copies are in flight, and
+ *     store the codes; the stage that holds the token is copied only after
+ *     the store), then the merge: two kernels (the fused append of HACK's
+ *     decode kernel and of VecInfer's 注意力机制中的向量量化KV缓存, where the new
+ *     code joins the cached ones).  For the 1.5-bit format (4096 centroids)
+ *     a kernel first scans each new vector's codebooks over several CTAs and
+ *     leaves their candidates in the workspace, which the attention kernel's
+ *     producers merge: three kernels;
  *   - otherwise three kernels: the append encode, the split attention (it
  *     starts while the append runs, prepares its tables, and waits for the
  *     append before it reads the pools) and the merge; with 10- to 12-bit
