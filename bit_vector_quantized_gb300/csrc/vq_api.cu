@@ -408,7 +408,8 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
   // budget), and 8 wherever 12 leaves room for fewer than kProducerWarps
   // stages; VQ_DECODE_SHAPE=8x1|12x1 selects a shape explicitly (a tuning
   // switch for profiling; an explicit shape that does not fit is an error).
-  vqk::DecodeShape shape = p.group > 4 ? vqk::DecodeShape{8} : vqk::DecodeShape{12};
+  // (the 1.5-bit format: 8, its whole-centroid gathers need the registers)
+  vqk::DecodeShape shape = (p.group > 4 || L.k_bits == 12) ? vqk::DecodeShape{8} : vqk::DecodeShape{12};
   bool explicit_shape = false;
   if (const char* env = std::getenv("VQ_DECODE_SHAPE")) {
     if (std::strcmp(env, "8x1") == 0) shape = vqk::DecodeShape{8}, explicit_shape = true;

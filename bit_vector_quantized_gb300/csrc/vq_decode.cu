@@ -84,6 +84,9 @@ __device__ __forceinline__ uint2 tab64(uint32_t off) {
 __device__ __forceinline__ uint32_t tab32(uint32_t off) {
   return *reinterpret_cast<const uint32_t*>(g_smem + off);
 }
+__device__ __forceinline__ uint4 tab128(uint32_t off) {
+  return *reinterpret_cast<const uint4*>(g_smem + off);
+}
 // Table offset of the 8-bit code in byte i of w: byte 1 of the result is the
 // code (the 256-byte row), byte 0 the lane's byte inside the row (lw < 256).
 __device__ __forceinline__ uint32_t row_addr(uint32_t w, uint32_t lw, int i) {
@@ -168,14 +171,12 @@ struct VCodes<2, 8> {
 };
 
 // d = 8, 12-bit codes (the pages' 1.5-bit configuration): the table is not
-// replicated.  A lane's 8-byte gather is half of one 8-element centroid, and
-// every lane of one gather reads the same half, so the table is half-major:
-// [tensor][half][code] x 8 bytes (K at 0, V at 64 KiB; half 1 at +32 KiB).
-// Consecutive codes then sit in consecutive bank pairs, and the random codes
-// of a warp spread over all 16 of them.
-__device__ __forceinline__ uint32_t row12(uint32_t code, uint32_t lw, int half) {
-  return (code << 3) | lw | (static_cast<uint32_t>(half) << 15);
-}
+// replicated (two 64 KiB tables, K at 0 and V at 64 KiB, one 16-byte row of
+// fp16 elements per code).  A lane reads a whole centroid with one 16-byte
+// load, which serves two k-steps (K) or two output steps (V): a quarter-warp
+// phase of 8 random rows meets fewer bank conflicts than the half-warp phase
+// of two 8-byte loads.
+__device__ __forceinline__ uint32_t row16(uint32_t code, uint32_t lw) { return (code << 4) | lw; }
 template <>
 struct KCodes<8> {
   uint32_t a, b;  // the lane's 48-bit code group (sub-vectors 4c .. 4c+3), from bit 0
@@ -188,12 +189,11 @@ struct KCodes<8> {
     a = __funnelshift_r(lo, hi, sh);
     b = hi >> sh;
   }
-  // k-step i (0..7) reads half (i & 1) of sub-vector 4c + i / 2
-  __device__ __forceinline__ uint32_t off(int i, uint32_t lw) const {
-    const int j = i >> 1;
+  // sub-vector 4c + j (0..3): k-steps 2j (elements 0..3) and 2j + 1 (4..7)
+  __device__ __forceinline__ uint32_t off16(int j, uint32_t lw) const {
     const uint32_t code = j == 0 ? (a & 0xfffu) : j == 1 ? ((a >> 12) & 0xfffu)
                         : j == 2 ? (__funnelshift_r(a, b, 24) & 0xfffu) : ((b >> 4) & 0xfffu);
-    return row12(code, lw, i & 1);
+    return row16(code, lw);
   }
 };
 template <>
@@ -209,10 +209,9 @@ struct VCodes<8, 12> {
     const uint32_t hi = sh > 8 ? rw[w0 + 1] : 0u;
     x = __funnelshift_r(lo, hi, sh);
   }
-  // output step i (0..3): dims 16r + 4i .. 16r + 4i + 3 = half (i & 1) of sub-vector 2r + i / 2
-  __device__ __forceinline__ uint32_t off(int i, uint32_t lw) const {
-    const uint32_t code = (i >> 1) ? ((x >> 12) & 0xfffu) : (x & 0xfffu);
-    return row12(code, lw, i & 1);
+  // sub-vector 2r + m (m = 0, 1): output steps 2m (elements 0..3) and 2m + 1 (4..7)
+  __device__ __forceinline__ uint32_t off16(int m, uint32_t lw) const {
+    return row16(m ? ((x >> 12) & 0xfffu) : (x & 0xfffu), lw);
   }
 };
 
@@ -815,8 +814,8 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
 
   // ============================= consumer warps ==============================
   // Codebook table: row j = 16 copies of 8-byte (32 copies of 4-byte) K
-  // centroid j, then the same for V centroid j; the 1.5-bit format's table is
-  // half-major ([tensor][half][code] x 8 bytes, see row12), copied in one pass.
+  // centroid j, then the same for V centroid j; the 1.5-bit format's tables
+  // are the codebooks as they are (K at 0, V at 64 KiB, see row16).
   if constexpr (kWide) {
     const uint32_t tab = smem_addr(smem + L.tab);
     constexpr int kBatch = 4;  // loads in flight per thread
@@ -835,12 +834,9 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
         const int j = j0 + i * kConsumerThreads;
         if (j < (1 << BK)) {
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const uint32_t base = tab + t * 65536u + j * 8u;
-            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(base), "r"(kv[i][t].x), "r"(kv[i][t].y));
-            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(base + 32768u), "r"(kv[i][t].z),
-                         "r"(kv[i][t].w));
-          }
+          for (int t = 0; t < 2; ++t)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(tab + t * 65536u + j * 16u),
+                         "r"(kv[i][t].x), "r"(kv[i][t].y), "r"(kv[i][t].z), "r"(kv[i][t].w));
         }
       }
     }
@@ -1007,15 +1003,38 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   //  G > 4: reduction over 16 tokens, A = V^T built with PRMT (pairs of tokens).
   // gather offsets: 256-byte table rows, or 128-byte rows for the table-based methods
   auto vgoff = [&](const VCodes<DV, BV>& v, int i) -> uint32_t {
-    if constexpr (kLut) return v.off7(i, lwv);
+    if constexpr (kWide) return 0u;  // the 1.5-bit format gathers whole centroids (off16)
+    else if constexpr (kLut) return v.off7(i, lwv);
     else return v.off(i, lwv);
   };
   auto kgoff = [&](const KCodes<DK>& kcd, int i) -> uint32_t {
-    if constexpr (kBins) return kcd.off7(i, lwk);
+    if constexpr (kWide) return 0u;
+    else if constexpr (kBins) return kcd.off7(i, lwk);
     else return kcd.off(i, lwk);
   };
+  uint4 vw[4];  // 1.5-bit format: the whole centroids of the current output-step pair
   auto pv_step = [&](int q) {
-    if constexpr (NG == 4) {
+    if constexpr (kWide) {
+      if ((q & 1) == 0) {
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) vw[jj] = tab128(pvc[jj].off16(q >> 1, lwv));
+      }
+      uint2 W[4];
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) W[jj] = (q & 1) ? make_uint2(vw[jj].z, vw[jj].w) : make_uint2(vw[jj].x, vw[jj].y);
+      if constexpr (NG == 4) {
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)  // tokens 8ks + c and 8ks + c + 4
+          mma16816(O[q], W[2 * ks].x, W[2 * ks].y, W[2 * ks + 1].x, W[2 * ks + 1].y, pb[ks][0], pb[ks][1]);
+      } else {
+        mma16816(O[2 * q], __byte_perm(W[0].x, W[1].x, sel_lo), __byte_perm(W[0].x, W[1].x, sel_hi),
+                 __byte_perm(W[2].x, W[3].x, sel_lo), __byte_perm(W[2].x, W[3].x, sel_hi), pb[0][0],
+                 pb[0][1]);
+        mma16816(O[2 * q + 1], __byte_perm(W[0].y, W[1].y, sel_lo), __byte_perm(W[0].y, W[1].y, sel_hi),
+                 __byte_perm(W[2].y, W[3].y, sel_lo), __byte_perm(W[2].y, W[3].y, sel_hi), pb[0][0],
+                 pb[0][1]);
+      }
+    } else if constexpr (NG == 4) {
 #pragma unroll
       for (int ks = 0; ks < 2; ++ks) {  // tokens 8ks + c and 8ks + c + 4
         uint32_t a0, a1, a2, a3;
@@ -1060,11 +1079,21 @@ __global__ void __launch_bounds__((NW + kProducerWarps) * 32, 1) vq_decode_split
   // chunk, two independent streams the scheduler interleaves.
   auto fused = [&](float (&sc)[4], bool with_qk) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+    uint4 kw0, kw1;  // 1.5-bit format: whole centroids of tokens r and r+8 for k-steps 2j, 2j+1
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       if (with_qk) {
         uint32_t a0, a1, a2, a3;
-        if constexpr (DK >= 4) {
+        if constexpr (kWide) {
+          if ((kk & 1) == 0) {
+            kw0 = tab128(kc[0].off16(kk >> 1, lwk));
+            kw1 = tab128(kc[1].off16(kk >> 1, lwk));
+          }
+          a0 = (kk & 1) ? kw0.z : kw0.x;
+          a1 = (kk & 1) ? kw1.z : kw1.x;
+          a2 = (kk & 1) ? kw0.w : kw0.y;
+          a3 = (kk & 1) ? kw1.w : kw1.y;
+        } else if constexpr (DK >= 4) {
           const uint2 g0 = tab64(kgoff(kc[0], kk));
           const uint2 g1 = tab64(kgoff(kc[1], kk));
           a0 = g0.x; a1 = g1.x; a2 = g0.y; a3 = g1.y;
