@@ -90,3 +90,17 @@ def test_reference_arm_rank0_prints_one_line():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_step_launch_counts_follow_the_documented_forms():
+    # bench.py's gpu_launches claim: the kernels one vq_decode_step launches on
+    # each workload, per include/vqattn.h (fused append: 2; the 1.5-bit format
+    # with its sliced scan: 3; more pairs than SMs: 3)
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    got = {i: bench.step_launches(W.WORKLOADS[i], 152) for i in (1, 2, 3, 4, 5)}
+    assert got == {1: 2, 2: 2, 3: 2, 4: 3, 5: 3}
+    # a 1.5-bit batch with more (sequence, KV head) pairs than SMs: scan, merge, attention, merge
+    w = W.custom(batch=64, num_q_heads=32, num_kv_heads=8, k_sub=8, k_bits=12, v_sub=8, v_bits=12)
+    assert bench.step_launches(w, 152) == 4
