@@ -51,7 +51,8 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 CALIB_DIR = os.path.join(ROOT, "tests", "golden", "calib")
 KERNEL_SRCS = [os.path.join(ROOT, "bit_vector_quantized_gb300", "csrc", f)
-               for f in ("vq_decode.cu", "vq_device.cuh", "vq_kernels.h")]
+               for f in ("vq_decode_kernel.cuh", "vq_decode.cu", "vq_decode_balanced.cu",
+                         "vq_device.cuh", "vq_kernels.h")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
 
 

@@ -20,7 +20,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libvqattn.so")
-SOURCES = ["vq_api.cu", "vq_encode.cu", "vq_decode.cu", "vq_combine.cu", "vq_dequant.cu"]
+SOURCES = ["vq_api.cu", "vq_encode.cu", "vq_decode.cu", "vq_decode_balanced.cu", "vq_combine.cu",
+           "vq_dequant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE,
               "--expt-relaxed-constexpr"]

@@ -71,12 +71,44 @@ bool decode_formats_supported(const vq_layout& L) {
 constexpr int kMaxSplits = 4096;
 constexpr int kMaxResidual = 4096;  // residual window capacity (tokens)
 
-// Split count minimising an estimate of the persistent grid's makespan:
-// waves(units) * (tokens per unit + fixed per-unit cost).
+// Smallest length-balanced position range per CTA: a pair's
+// ceil(max_seq_len / 32) blocks then meet at most `splits` CTAs.
+int balance_wmin(int max_seq_len, int splits) {
+  const int nsl = (max_seq_len + vqk::kUnitTok - 1) / vqk::kUnitTok;
+  return (nsl + splits - 2) / (splits - 1);
+}
+
+// Length-balanced units (decode kernel, DecodeParams::balanced) for batches
+// of two or more sequences: the grid (one CTA per SM) splits the pairs' blocks
+// evenly whatever the lengths.  Needs two or more partial slots per pair and
+// at most kMaxUnitsPerCta units per CTA, which holds with at most that many
+// pairs or with a per-CTA range W <= (kMaxUnitsPerCta - 2) (1 + kBalanceGap)
+// (pairs after a CTA's first start inside its range, 1 + kBalanceGap
+// positions apart at least).
+bool balanced_units(const vq_layout& L, int batch, int max_seq_len, int splits, int sms) {
+  if (batch < 2 || batch > vqk::kBalanceMaxBatch || splits < 2 || sms <= 0 || max_seq_len < 1) return false;
+  const long long pairs = static_cast<long long>(batch) * L.num_kv_heads;
+  const long long nsl = (static_cast<long long>(max_seq_len) + vqk::kUnitTok - 1) / vqk::kUnitTok;
+  const long long total = pairs * (nsl + vqk::kBalanceGap);  // the largest total the kernel can see
+  if (total >= (1LL << 30)) return false;
+  const long long w = std::max<long long>((total + sms - 1) / sms, balance_wmin(max_seq_len, splits));
+  return pairs <= vqk::kMaxUnitsPerCta ||
+         w <= static_cast<long long>(vqk::kMaxUnitsPerCta - 2) * (1 + vqk::kBalanceGap);
+}
+
+// Split count.  Batches of two or more sequences: length-balanced units with
+// 1 + ceil(2 SMs / pairs) slots per pair (a pair may be twice the average
+// length before bal_wmin, rather than the lengths, sets the CTA range).
+// Otherwise the count minimising an estimate of the persistent grid's
+// makespan: waves(units) * (tokens per unit + fixed per-unit cost).
 int pick_splits(const vq_layout& L, int batch, int max_seq_len, int sms) {
   const long long pairs = static_cast<long long>(batch) * L.num_kv_heads;
   const long long chunks = (static_cast<long long>(max_seq_len) + 15) / 16;
   if (pairs <= 0 || chunks <= 0 || sms <= 0) return 1;
+  if (batch >= 2) {
+    const int sb = static_cast<int>(std::min<long long>(1 + (2LL * sms + pairs - 1) / pairs, kMaxSplits));
+    if (balanced_units(L, batch, max_seq_len, sb, sms)) return sb;
+  }
   const double kUnitOverhead = 384.0;  // tokens-equivalent per unit (q~, merge, pipeline fill)
   int best = 1;
   double best_cost = 1e300;
@@ -100,16 +132,18 @@ int pick_splits(const vq_layout& L, int batch, int max_seq_len, int sms) {
 bool sliced_append(const vq_layout& L) { return L.k_bits >= 10 || L.v_bits >= 10; }
 
 struct WsLayout {
-  size_t o_off, ml_off, cand_off, total;
+  size_t o_off, ml_off, cnt_off, cand_off, total;
 };
 
-// Split partials, then (large codebooks) the sliced append's candidates.
+// Split partials, the units per (sequence, KV head) of length-balanced
+// units, then (large codebooks) the sliced append's candidates.
 WsLayout ws_layout(const vq_layout& L, int batch, int splits) {
   WsLayout w;
   const size_t rows = static_cast<size_t>(batch) * L.num_q_heads * splits;
   w.o_off = 0;
   w.ml_off = (rows * L.head_dim * sizeof(float) + 255) & ~size_t(255);
-  w.cand_off = w.ml_off + ((rows * 2 * sizeof(float) + 255) & ~size_t(255));
+  w.cnt_off = w.ml_off + ((rows * 2 * sizeof(float) + 255) & ~size_t(255));
+  w.cand_off = w.cnt_off + ((static_cast<size_t>(batch) * L.num_kv_heads * sizeof(int) + 255) & ~size_t(255));
   const size_t cand = sliced_append(L) ? static_cast<size_t>(batch) * L.num_kv_heads * 2 *
                                              vqk::kAppendSlices * 32 * 4 * sizeof(int2)
                                        : 0;
@@ -343,9 +377,10 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
     return fail(VQ_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, ws.total);
   const long long units = static_cast<long long>(batch) * L.num_kv_heads * splits;
   if (units > 0x7fffffffLL) return fail(VQ_ERR_INVALID_ARG, "too many work units");
+  const bool balanced = balanced_units(L, batch, max_seq_len, splits, sms);
   long long g = std::min<long long>(units, sms);
   g = std::max<long long>(g, (units + vqk::kMaxUnitsPerCta - 1) / vqk::kMaxUnitsPerCta);
-  grid = static_cast<int>(g);
+  grid = static_cast<int>(balanced ? sms : g);
 
   p = vqk::DecodeParams{};
   p.q = q;
@@ -374,13 +409,18 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
   const int nsl = (max_seq_len + vqk::kUnitTok - 1) / vqk::kUnitTok;
   p.split_q = nsl / splits;
   p.split_r = nsl % splits;
+  p.balanced = balanced ? 1 : 0;
+  p.bal_wmin = balanced ? balance_wmin(max_seq_len, splits) : 0;
+  p.ws_cnt = balanced ? reinterpret_cast<int*>(wsb + ws.cnt_off) : nullptr;
   p.k_row = static_cast<int>(vq_code_row_bytes(L.head_dim, L.k_sub, L.k_bits));
   p.v_row = static_cast<int>(vq_code_row_bytes(L.head_dim, L.v_sub, L.v_bits));
   const float scale = softmax_scale == 0.f ? 1.f / std::sqrt(static_cast<float>(L.head_dim)) : softmax_scale;
   p.qscale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 / std::sqrt(128.0));
   // residual window: a unit's slice is at most ceil(capacity / splits)
-  // tokens, staged in shared memory up to kMaxResTok at a time
-  const int res_tok = res_capacity > 0 ? std::min((res_capacity + splits - 1) / splits, vqk::kMaxResTok) : 0;
+  // tokens (length-balanced units: the whole window), staged in shared
+  // memory up to kMaxResTok at a time
+  const int res_slice = balanced ? res_capacity : (res_capacity + splits - 1) / splits;
+  const int res_tok = res_capacity > 0 ? std::min(res_slice, vqk::kMaxResTok) : 0;
   p.res_tok = res_tok;
 
   const int optin = device_smem_optin();
@@ -471,11 +511,12 @@ vq_status combine_impl(const vq_layout* layout, int32_t batch, int32_t max_seq_l
     return fail(VQ_ERR_INVALID_ARG, "workspace or out is not 16-byte aligned");
   if (num_splits > kMaxSplits) return fail(VQ_ERR_INVALID_ARG, "num_splits %d > %d", num_splits, kMaxSplits);
   int splits = num_splits;
-  if (splits <= 0) {
-    const int sms = device_sms();
+  int sms = 0;
+  if (splits <= 0 || batch >= 2) {  // the split choice, or whether the units were length-balanced
+    sms = device_sms();
     if (sms <= 0) return fail(VQ_ERR_CUDA, "no CUDA device");
-    splits = pick_splits(L, batch, max_seq_len, sms);
   }
+  if (splits <= 0) splits = pick_splits(L, batch, max_seq_len, sms);
   const WsLayout ws = ws_layout(L, batch, splits);
   if (workspace_bytes < ws.total)
     return fail(VQ_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, ws.total);
@@ -486,6 +527,9 @@ vq_status combine_impl(const vq_layout* layout, int32_t batch, int32_t max_seq_l
   cp.out = out;
   cp.rows = batch * L.num_q_heads;
   cp.splits = splits;
+  cp.cnt = balanced_units(L, batch, max_seq_len, splits, sms) ? reinterpret_cast<const int*>(wsb + ws.cnt_off)
+                                                               : nullptr;
+  cp.group = L.num_q_heads / L.num_kv_heads;
   cudaError_t e = vqk::launch_combine(cp, static_cast<cudaStream_t>(stream), overlap);
   if (e != cudaSuccess) return cuda_fail(e, "decode combine kernel");
   return VQ_OK;

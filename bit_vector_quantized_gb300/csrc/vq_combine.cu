@@ -16,14 +16,17 @@ namespace {
 // outputs of a chunk of up to 32 splits before using any (one round trip to
 // L2, bypassing L1: the partials were written by the previous kernel), then
 // merges them; chunks after the first rescale the running sums.  With at most
-// kC splits the sums are formed in split order from the global maximum.
-template <int kC>
+// kC splits the sums are formed in split order from the global maximum.  With
+// length-balanced units a row's pair has cnt <= splits partials (slots
+// 0 .. cnt-1); the other slots are loaded with them but left out.
+template <int kC, bool kCounted>
 __global__ void __launch_bounds__(kHeadDim) vq_combine_kernel(const CombineParams p) {
   const int row = blockIdx.x, d = threadIdx.x;
   pdl_trigger();
   pdl_wait();
   const float2* ml = p.ws_ml + static_cast<long long>(row) * p.splits;
   const float* o = p.ws_o + static_cast<long long>(row) * p.splits * kHeadDim + d;
+  const int cnt = kCounted ? __ldcg(p.cnt + row / p.group) : p.splits;
   float M = -INFINITY, acc = 0.f, l = 0.f;
   for (int s0 = 0; s0 < p.splits; s0 += kC) {
     float2 v[kC];
@@ -36,6 +39,15 @@ __global__ void __launch_bounds__(kHeadDim) vq_combine_kernel(const CombineParam
       if (sp < p.splits) {
         v[i] = __ldcg(ml + sp);
         ov[i] = __ldcg(o + static_cast<long long>(sp) * kHeadDim);
+      }
+    }
+    if constexpr (kCounted) {
+#pragma unroll
+      for (int i = 0; i < kC; ++i) {
+        if (s0 + i >= cnt) {
+          v[i] = make_float2(-INFINITY, 0.f);
+          ov[i] = 0.f;
+        }
       }
     }
     float Mc = M;
@@ -63,8 +75,10 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool ove
   if (p.rows == 0) return cudaSuccess;
   // chunk of partials loaded at once: the smallest of 4, 8, 16, 32 that holds them all
   const int terms = p.splits;
-  auto kern = terms <= 4 ? vq_combine_kernel<4> : terms <= 8 ? vq_combine_kernel<8>
-            : terms <= 16 ? vq_combine_kernel<16> : vq_combine_kernel<32>;
+  auto kern = p.cnt ? (terms <= 4 ? vq_combine_kernel<4, true> : terms <= 8 ? vq_combine_kernel<8, true>
+                       : terms <= 16 ? vq_combine_kernel<16, true> : vq_combine_kernel<32, true>)
+                    : (terms <= 4 ? vq_combine_kernel<4, false> : terms <= 8 ? vq_combine_kernel<8, false>
+                       : terms <= 16 ? vq_combine_kernel<16, false> : vq_combine_kernel<32, false>);
   cudaError_t e = launch_pdl(kern, dim3(p.rows), dim3(kHeadDim), 0, stream, p, overlap);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

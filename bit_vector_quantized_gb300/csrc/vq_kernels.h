@@ -60,6 +60,16 @@ struct DecodeParams {
   int page_size, max_pages, max_seq_len;
   int splits, num_units;
   int split_q, split_r;       // ceil(max_seq_len / 32) = split_q * splits + split_r
+  // Length-balanced units (balanced != 0, batches of two or more sequences):
+  // the (sequence, KV head) pairs are laid end to end, each as its 32-token
+  // blocks followed by kBalanceGap positions standing for a unit's fixed
+  // cost, and CTA c takes positions [c W, (c + 1) W) with
+  // W = max(ceil(total / grid), bal_wmin).  The blocks of a pair that fall in
+  // one CTA form a unit; the pair's j-th unit writes partial slot j, and its
+  // first writes the pair's unit count to ws_cnt.  bal_wmin keeps the units
+  // of a pair within `splits` slots.
+  int balanced, bal_wmin;
+  int* ws_cnt;                // [B][Hkv] units per pair (balanced)
   int k_row, v_row;
   int nstage;
   int warps;                  // consumer warps (DecodeShape)
@@ -111,12 +121,16 @@ struct CombineParams {
   void* out;                  // fp16 [B][Hq][128]
   int rows;                   // B * Hq
   int splits;
+  const int* cnt;             // [B][Hkv] partials per pair (length-balanced units), or NULL: `splits`
+  int group;                  // Hq / Hkv (row / group = pair)
 };
 
 
 constexpr int kProducerWarps = 4;  // TMA-issuing warps (one in four stages each)
 constexpr int kMaxUnitsPerCta = 256;
 constexpr int kUnitTok = 32;       // split boundaries are multiples of this many tokens
+constexpr int kBalanceGap = 12;    // a unit's fixed cost in 32-token blocks (length-balanced units)
+constexpr int kBalanceMaxBatch = 512;  // sequences, at most, for length-balanced units
 
 constexpr int kMaxResTok = 64;     // residual window tokens staged in shared memory at a time, at most
 constexpr int kMaxStages = 16;     // pipeline slots of the split kernel, at most
@@ -188,7 +202,7 @@ __host__ __device__ inline DecodeSmem decode_smem(int k_bits, int v_bits, int gr
   s.units = o; o = align128(o + 3 * kMaxUnitsPerCta * 4);  // lengths (consumers, producers), window lengths
   s.meta = o; o = align128(o + nstage * 16);
   s.bar = o; o = align128(o + (nstage * 2 + 1) * 8);  // full and empty per slot, then the append's
-  s.flag = o; o = align128(o + 16);
+  s.flag = o; o = align128(o + 64);  // abort flag, then the CTA's length-balanced unit range
   s.enc = o; o = align128(o + append_enc);
   s.aux = o; o = align128(o + (method ? kLutBytes : 0) + (method == 2 ? (1 << v_bits) * 4 * 4 : 0));
   s.res = s.merge;
@@ -259,9 +273,13 @@ cudaError_t launch_encode_merge(const EncodeParams& p, int vectors, int grid_y, 
 constexpr int kAppendSlices = 8;  // CTAs per vector for appends with 1024 or more centroids
 
 // Returns cudaErrorInvalidValue when no kernel is compiled for the formats.
+// launch_decode takes either assignment (p.balanced); launch_decode_balanced
+// is its length-balanced half.
 cudaError_t launch_decode(const DecodeParams& p, int k_sub, int k_bits, int v_sub, int v_bits,
                           int grid, size_t smem, cudaStream_t stream, bool overlap,
                           int method = kMethodGather);
+cudaError_t launch_decode_balanced(const DecodeParams& p, int k_sub, int k_bits, int v_sub, int v_bits,
+                                   int grid, size_t smem, cudaStream_t stream, bool overlap, int method);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool overlap);
 cudaError_t launch_dequant(const DequantParams& p, int grid_x, cudaStream_t stream);
 int dequant_tokens_per_cta();

@@ -76,6 +76,27 @@ def test_split_heuristic_and_workspace(lib):
     assert vq.vq_decode_workspace_bytes(L1, -1, 10, 0, 152) == 0
 
 
+def _up256(x):
+    return (x + 255) // 256 * 256
+
+
+def test_length_balanced_split_counts_and_workspace(lib):
+    """Two or more sequences get length-balanced units with 1 + ceil(2 SMs /
+    pairs) partial slots per (sequence, KV head); the workspace holds the
+    partials, then one int32 unit count per pair."""
+    L1 = vq.make_layout()                                                  # 8 KV heads
+    assert vq.vq_default_num_splits(L1, 16, 8193, 152) == 1 + 3            # 128 pairs
+    assert vq.vq_default_num_splits(L1, 2, 32769, 152) == 1 + 19           # 16 pairs
+    L4 = vq.make_layout(num_q_heads=40, k_sub=2, v_bits=9)
+    assert vq.vq_default_num_splits(L4, 64, 16385, 152) == 2               # 512 pairs
+    # more sequences than the balanced assignment takes: the fixed-split heuristic
+    s = vq.vq_default_num_splits(L1, 600, 100, 152)
+    assert s >= 1
+    rows = 3 * 32 * 19
+    assert vq.vq_decode_workspace_bytes(L1, 3, 32769, 19, 152) == \
+        _up256(rows * 128 * 4) + _up256(rows * 2 * 4) + _up256(3 * 8 * 4)
+
+
 FAKE = 1 << 20  # 16-byte aligned, never dereferenced: validation fails first
 
 

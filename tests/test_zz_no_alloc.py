@@ -63,13 +63,13 @@ def test_static_scratch_matches_workspace_path_twice():
 
 def test_static_scratch_lowers_the_default_split_count_to_fit():
     """With num_splits <= 0 the library's split choice is lowered until the
-    partials fit the array.  Batch 32 x 64 query heads over 8 KV heads at 8K
-    context takes 4 splits on a 152-SM GB300, 4.06 MiB of partials; the call
-    runs at 3 splits, bit-identical to the workspace path at that count.
-    Seeded random codes stand in for a filled cache (the result is only
-    compared between the two paths)."""
+    partials fit the array.  Batch 64 x 64 query heads over 8 KV heads at 4K
+    context takes 2 splits (length-balanced units) on a 152-SM GB300, just
+    over 4 MiB of partials; the call runs at 1 split, bit-identical to the
+    workspace path at that count.  Seeded random codes stand in for a filled
+    cache (the result is only compared between the two paths)."""
     import bit_vector_quantized_gb300 as vq
-    w = W.custom(name="static-big", batch=32, num_q_heads=64, num_kv_heads=8, context=8192,
+    w = W.custom(name="static-big", batch=64, num_q_heads=64, num_kv_heads=8, context=4096,
                  k_sub=4, v_sub=4, page_size=256)
     cal = calib_for(w)
     gc = GpuCache(w, cal)
