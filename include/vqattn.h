@@ -175,18 +175,25 @@ vq_status vq_dequantize_kv(const vq_layout* layout, int32_t num_tokens,
 /*
  * Workspace bytes vq_decode_attention (and vq_decode_step) needs for `batch`
  * sequences split `num_splits` ways (num_splits <= 0: the value
- * vq_default_num_splits picks): the split partials, and for codebooks of 1024
- * centroids or more (10- to 12-bit codes) also the candidates of
- * vq_decode_step's append, which spreads each new vector's codebook scan over
- * several CTAs.  Pure host arithmetic.  Returns 0 for invalid arguments.
+ * vq_default_num_splits picks): the split partials, one int32 per
+ * (sequence, KV head) for the partial count of length-balanced units, and
+ * for codebooks of 1024 centroids or more (10- to 12-bit codes) also the
+ * candidates of vq_decode_step's append, which spreads each new vector's
+ * codebook scan over several CTAs.  Pure host arithmetic.  Returns 0 for
+ * invalid arguments.
  */
 size_t vq_decode_workspace_bytes(const vq_layout* layout, int32_t batch,
                                  int32_t max_seq_len, int32_t num_splits, int32_t num_sms);
 
 /*
- * Split-K factor the library picks for a batch: the number of sequence
- * splits per (sequence, KV head) that balances work units over num_sms SMs
- * (num_sms <= 0: query the current device).  Returns >= 1, or 0 on error.
+ * Split-K factor the library picks for a batch (num_sms <= 0: query the
+ * current device).  One sequence: the number of splits per (sequence, KV
+ * head) that balances work units over num_sms SMs.  Two or more sequences
+ * (up to 512): 1 + ceil(2 num_sms / (batch * Hkv)) partial slots per
+ * (sequence, KV head) for length-balanced units, where every SM gets an
+ * equal share of the batch's 32-token blocks whatever the lengths (the
+ * fixed-split count when that assignment's bounds do not hold).  Returns
+ * >= 1, or 0 on error.
  */
 int32_t vq_default_num_splits(const vq_layout* layout, int32_t batch, int32_t max_seq_len,
                               int32_t num_sms);
@@ -206,8 +213,12 @@ int32_t vq_default_num_splits(const vq_layout* layout, int32_t batch, int32_t ma
  *   max_seq_len  host upper bound of seq_lens, used to size the split grid;
  *                tokens beyond it are ignored.
  *   softmax_scale multiplies the scores; 0 selects 1/sqrt(D).
- *   num_splits   sequence splits per (sequence, KV head); <= 0 selects the
- *                library's choice.  Results do not depend on it beyond
+ *   num_splits   partials per (sequence, KV head); <= 0 selects the
+ *                library's choice.  With one sequence (or num_splits 1) each
+ *                sequence is cut into num_splits ranges of max_seq_len;
+ *                with two or more, the batch's blocks are divided evenly
+ *                over the SMs and a (sequence, KV head) meets at most
+ *                num_splits of them.  Results do not depend on it beyond
  *                fp32 rounding.
  *   out          fp16 [batch][Hq][D] attention output.
  *   workspace    device scratch of at least vq_decode_workspace_bytes(...)
