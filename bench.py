@@ -611,12 +611,13 @@ def encode_report(w, tokens, ms, sms, clocks):
                          "algorithmic_fma_per_token_head": ((1 << w.k_bits) + (1 << w.v_bits)) * w.head_dim}}
 
 
-def workload_config(w, splits, copies):
+def workload_config(w, splits, copies, balanced=None):
     return {"workload": w.name, "batch": w.batch, "q_heads": w.num_q_heads,
             "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "context": w.context,
             "attended_tokens_per_step": tokens_per_step(w),
             "k_code": f"d{w.k_sub} x {w.k_bits}-bit", "v_code": f"d{w.v_sub} x {w.v_bits}-bit",
             "page_size": w.page_size, "num_splits": splits,
+            "units": None if balanced is None else ("length-balanced" if balanced else "fixed splits"),
             "l2": (f"rotating {copies} cache copies ({copies * code_bytes_per_step(w) / 1e6:.0f} MB"
                    " of codes) > 2x L2" if copies else None)}
 
@@ -961,7 +962,7 @@ def main():
         cpu = run_cpu_baseline(w, lam, ck, cv, args.cpu_seconds)
 
     if rank == 0:
-        cfg = workload_config(w, splits, copies)
+        cfg = workload_config(w, splits, copies, vq.vq_decode_units_balanced(layout, B, max_len, splits) == 1)
         cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
         cfg["graph"] = True
         line = {

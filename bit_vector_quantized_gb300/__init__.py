@@ -32,7 +32,8 @@ VQ_DEV_OK, VQ_DEV_BAD_PAGE, VQ_DEV_BAD_SLOT, VQ_DEV_TIMEOUT, VQ_DEV_BAD_CONFIG =
 
 # every symbol include/vqattn.h declares
 EXPORTED = ("vq_code_row_bytes", "vq_check_layout", "vq_encode_kv", "vq_decode_workspace_bytes",
-            "vq_default_num_splits", "vq_decode_attention", "vq_decode_partial",
+            "vq_default_num_splits", "vq_decode_units_balanced", "vq_decode_attention",
+            "vq_decode_partial",
             "vq_decode_partial_method", "vq_decode_combine", "vq_decode_step", "vq_dequantize_kv",
             "vq_decode_residual_workspace_bytes", "vq_decode_attention_residual",
             "vq_decode_attention_static", "vq_static_scratch_bytes", "vq_last_error",
@@ -84,6 +85,7 @@ def lib() -> ctypes.CDLL:
                                                    P, P]),
             "vq_decode_workspace_bytes": (SZ, [LP, I32, I32, I32, I32]),
             "vq_default_num_splits": (I32, [LP, I32, I32, I32]),
+            "vq_decode_units_balanced": (I32, [LP, I32, I32, I32, I32]),
             "vq_decode_attention": (I32, [LP, I32, P, P, P, P, P, P, I64, P, I32, P, I32,
                                           ctypes.c_float, I32, P, P, SZ, P, P]),
             "vq_decode_partial": (I32, [LP, I32, P, P, P, P, P, P, I64, P, I32, P, I32,
@@ -167,6 +169,11 @@ def vq_decode_workspace_bytes(layout, batch, max_seq_len, num_splits=0, num_sms=
 
 def vq_default_num_splits(layout, batch, max_seq_len, num_sms=0) -> int:
     return int(lib().vq_default_num_splits(ctypes.byref(layout), batch, max_seq_len, num_sms))
+
+
+def vq_decode_units_balanced(layout, batch, max_seq_len, num_splits=0, num_sms=0) -> int:
+    return int(lib().vq_decode_units_balanced(ctypes.byref(layout), batch, max_seq_len,
+                                              num_splits, num_sms))
 
 
 def vq_decode_attention(layout, batch, q, lambda_, codebook_k, codebook_v, k_pool, v_pool,

@@ -331,6 +331,16 @@ int32_t vq_default_num_splits(const vq_layout* layout, int32_t batch, int32_t ma
   return pick_splits(*layout, batch, max_seq_len, sms);
 }
 
+int32_t vq_decode_units_balanced(const vq_layout* layout, int32_t batch, int32_t max_seq_len,
+                                 int32_t num_splits, int32_t num_sms) {
+  if (!layout || batch < 0 || max_seq_len < 0 || layout->num_kv_heads < 1) return -1;
+  if (num_splits > kMaxSplits) return -1;
+  const int sms = num_sms > 0 ? num_sms : device_sms();
+  if (sms <= 0) return -1;
+  const int splits = num_splits > 0 ? num_splits : pick_splits(*layout, batch, max_seq_len, sms);
+  return balanced_units(*layout, batch, max_seq_len, splits, sms) ? 1 : 0;
+}
+
 size_t vq_decode_workspace_bytes(const vq_layout* layout, int32_t batch, int32_t max_seq_len,
                                  int32_t num_splits, int32_t num_sms) {
   if (!layout || batch < 0 || max_seq_len < 0 || layout->num_q_heads < 1) return 0;

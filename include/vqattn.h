@@ -199,6 +199,18 @@ int32_t vq_default_num_splits(const vq_layout* layout, int32_t batch, int32_t ma
                               int32_t num_sms);
 
 /*
+ * How the decode kernels divide the work of `batch` sequences for these
+ * arguments (num_splits <= 0: vq_default_num_splits' choice; num_sms <= 0:
+ * the current device): 1 for length-balanced units (the batch's 32-token
+ * blocks divided evenly over the SMs; a (sequence, KV head) then has between
+ * 1 and num_splits partials), 0 for fixed splits (num_splits ranges of
+ * max_seq_len per sequence).  Pure host arithmetic.  Returns -1 for invalid
+ * arguments.
+ */
+int32_t vq_decode_units_balanced(const vq_layout* layout, int32_t batch, int32_t max_seq_len,
+                                 int32_t num_splits, int32_t num_sms);
+
+/*
  * Decode attention for one query token per sequence over the quantized cache
  * (VecInfer, section 方法细节 "注意力机制中的向量量化KV缓存"; split-K with an
  * online-softmax merge as in the FlashAttention recurrence of the appendix

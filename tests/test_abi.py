@@ -92,6 +92,14 @@ def test_length_balanced_split_counts_and_workspace(lib):
     # more sequences than the balanced assignment takes: the fixed-split heuristic
     s = vq.vq_default_num_splits(L1, 600, 100, 152)
     assert s >= 1
+    assert vq.vq_decode_units_balanced(L1, 600, 100, 0, 152) == 0
+    assert vq.vq_decode_units_balanced(L1, 16, 8193, 0, 152) == 1
+    assert vq.vq_decode_units_balanced(L1, 1, 32769, 0, 152) == 0         # one sequence: fixed splits
+    assert vq.vq_decode_units_balanced(L1, 16, 8193, 1, 152) == 0         # one slot per pair
+    assert vq.vq_decode_units_balanced(L1, 16, 0, 0, 152) == 0            # nothing to attend
+    assert vq.vq_decode_units_balanced(L1, -1, 10, 0, 152) == -1
+    # 512 sequences x 8 KV heads of 1M tokens: too many units per CTA for the balanced bound
+    assert vq.vq_decode_units_balanced(L1, 512, 1 << 20, 4, 152) == 0
     rows = 3 * 32 * 19
     assert vq.vq_decode_workspace_bytes(L1, 3, 32769, 19, 152) == \
         _up256(rows * 128 * 4) + _up256(rows * 2 * 4) + _up256(3 * 8 * 4)
