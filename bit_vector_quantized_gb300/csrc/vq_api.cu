@@ -71,8 +71,9 @@ bool decode_formats_supported(const vq_layout& L) {
 constexpr int kMaxSplits = 4096;
 constexpr int kMaxResidual = 4096;  // residual window capacity (tokens)
 
-// Smallest length-balanced position range per CTA: a pair's
-// ceil(max_seq_len / 32) blocks then meet at most `splits` CTAs.
+// Largest value the length-balanced kernel's slot term of W,
+// ceil(longest pair's blocks / (splits - 1)), can take: the pairs' blocks
+// are at most ceil(max_seq_len / 32).
 int balance_wmin(int max_seq_len, int splits) {
   const int nsl = (max_seq_len + vqk::kUnitTok - 1) / vqk::kUnitTok;
   return (nsl + splits - 2) / (splits - 1);
@@ -84,7 +85,8 @@ int balance_wmin(int max_seq_len, int splits) {
 // at most kMaxUnitsPerCta units per CTA, which holds with at most that many
 // pairs or with a per-CTA range W <= (kMaxUnitsPerCta - 2) (1 + kBalanceGap)
 // (pairs after a CTA's first start inside its range, 1 + kBalanceGap
-// positions apart at least).
+// positions apart at least); the kernel's W is at most the bound taken here
+// from max_seq_len.
 bool balanced_units(const vq_layout& L, int batch, int max_seq_len, int splits, int sms) {
   if (batch < 2 || batch > vqk::kBalanceMaxBatch || splits < 2 || sms <= 0 || max_seq_len < 1) return false;
   const long long pairs = static_cast<long long>(batch) * L.num_kv_heads;
@@ -98,7 +100,7 @@ bool balanced_units(const vq_layout& L, int batch, int max_seq_len, int splits, 
 
 // Split count.  Batches of two or more sequences: length-balanced units with
 // 1 + ceil(2 SMs / pairs) slots per pair (a pair may be twice the average
-// length before bal_wmin, rather than the lengths, sets the CTA range).
+// length before the slot term, rather than the total, sets the CTA range).
 // Otherwise the count minimising an estimate of the persistent grid's
 // makespan: waves(units) * (tokens per unit + fixed per-unit cost).
 int pick_splits(const vq_layout& L, int batch, int max_seq_len, int sms) {
@@ -420,7 +422,6 @@ vq_status prepare_decode(const vq_layout* layout, int32_t batch, const void* q, 
   p.split_q = nsl / splits;
   p.split_r = nsl % splits;
   p.balanced = balanced ? 1 : 0;
-  p.bal_wmin = balanced ? balance_wmin(max_seq_len, splits) : 0;
   p.ws_cnt = balanced ? reinterpret_cast<int*>(wsb + ws.cnt_off) : nullptr;
   p.k_row = static_cast<int>(vq_code_row_bytes(L.head_dim, L.k_sub, L.k_bits));
   p.v_row = static_cast<int>(vq_code_row_bytes(L.head_dim, L.v_sub, L.v_bits));

@@ -343,7 +343,10 @@ __device__ __forceinline__ bool append_attended(const DecodeParams& p, int t_beg
 // in shared memory, pre: room for batch + 1 prefix sums).  Pair (b, kvh) sits
 // at position Q = pre[b] + kvh (nb_b + gap) and occupies max(nb_b, 1)
 // positions from there (nb_b: its 32-token blocks); CTA c takes the pairs
-// that meet [c W, (c + 1) W).
+// that meet [c W, (c + 1) W), W = max(ceil(total / grid), ceil(max_b nb_b /
+// (splits - 1))): the second term keeps every pair within `splits` CTAs, and
+// taking the batch's own longest sequence (not max_seq_len) keeps a short
+// batch spread over the grid when max_seq_len is a loose bound.
 __device__ __forceinline__ void balance_units(const DecodeParams& p, const int* lens, int* pre, int* bal,
                                               int lane) {
   auto blocks = [&](int b) {
@@ -352,8 +355,13 @@ __device__ __forceinline__ void balance_units(const DecodeParams& p, const int* 
   };
   const int B = p.batch, per = (B + 31) / 32;
   const int b_lo = min(lane * per, B), b_hi = min(b_lo + per, B);
-  int sum = 0;
-  for (int b = b_lo; b < b_hi; ++b) sum += p.hkv * (blocks(b) + kBalanceGap);
+  int sum = 0, nb_max = 0;
+  for (int b = b_lo; b < b_hi; ++b) {
+    const int nb = blocks(b);
+    sum += p.hkv * (nb + kBalanceGap);
+    nb_max = max(nb_max, nb);
+  }
+  nb_max = __reduce_max_sync(kFull, nb_max);
   int incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -368,7 +376,7 @@ __device__ __forceinline__ void balance_units(const DecodeParams& p, const int* 
   __syncwarp();
   const long long total = __shfl_sync(kFull, incl, 31);
   const long long grid = gridDim.x, c = blockIdx.x;
-  const long long W = max((total + grid - 1) / grid, static_cast<long long>(p.bal_wmin));
+  const long long W = max((total + grid - 1) / grid, static_cast<long long>((nb_max + p.splits - 2) / (p.splits - 1)));
   const long long x0 = c * W, x1 = x0 + W;
   const int pairs = B * p.hkv;
   auto pos = [&](int pr) -> long long {

@@ -64,11 +64,12 @@ struct DecodeParams {
   // the (sequence, KV head) pairs are laid end to end, each as its 32-token
   // blocks followed by kBalanceGap positions standing for a unit's fixed
   // cost, and CTA c takes positions [c W, (c + 1) W) with
-  // W = max(ceil(total / grid), bal_wmin).  The blocks of a pair that fall in
-  // one CTA form a unit; the pair's j-th unit writes partial slot j, and its
-  // first writes the pair's unit count to ws_cnt.  bal_wmin keeps the units
-  // of a pair within `splits` slots.
-  int balanced, bal_wmin;
+  // W = max(ceil(total / grid), ceil(longest pair's blocks / (splits - 1))).
+  // The blocks of a pair that fall in one CTA form a unit; the pair's j-th
+  // unit writes partial slot j, and its first writes the pair's unit count
+  // to ws_cnt.  The second term of W keeps the units of a pair within
+  // `splits` slots.
+  int balanced;
   int* ws_cnt;                // [B][Hkv] units per pair (balanced)
   int k_row, v_row;
   int nstage;

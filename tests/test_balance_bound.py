@@ -4,11 +4,12 @@ When the library reports length-balanced units for a call
 (vq_decode_units_balanced == 1), the decode kernel lays the (sequence, KV
 head) pairs end to end (each pair's 32-token blocks followed by a 12-block gap
 standing for a unit's fixed cost), and CTA c of a grid of one CTA per SM takes
-positions [c W, (c + 1) W) with W = max(ceil(total / grid), ceil(blocks /
-(S - 1))).  The kernel keeps at most 256 units per CTA and S partial slots per
-pair.  These tests restate that rule with numpy and check, on adversarial
-length mixes, that every shape the library accepts keeps both limits, and that
-every block of every pair lands in exactly one CTA.
+positions [c W, (c + 1) W) with W = max(ceil(total / grid), ceil(longest
+pair's blocks / (S - 1))).  The kernel keeps at most 256 units per CTA and S
+partial slots per pair.  These tests restate that rule with numpy and check,
+on adversarial length mixes, that every shape the library accepts keeps both
+limits, that every block of every pair lands in exactly one CTA, and that a
+short batch under a loose max_seq_len stays spread over the grid.
 """
 import numpy as np
 import pytest
@@ -31,8 +32,7 @@ def _assign(lens, hkv, max_seq_len, splits, grid):
     q = np.concatenate([[0], np.cumsum(cost)[:-1]])
     ext = np.maximum(nb_pair, 1)
     total = int(cost.sum())
-    nsl = (max_seq_len + 31) // 32
-    w = max(-(-total // grid), -(-nsl // (splits - 1)))
+    w = max(-(-total // grid), -(-int(nb_pair.max()) // (splits - 1)))
     c = np.arange(grid, dtype=np.int64)
     x0, x1 = c * w, (c + 1) * w
     pa = np.searchsorted(q + ext, x0, side="right")   # first pair with q + ext > x0
@@ -91,3 +91,14 @@ def test_every_block_in_one_cta(lib):
         per_cta = np.bincount(owner, minlength=152)
         assert per_cta.max() <= w                    # no CTA gets more than its range
         assert int(per_cta.sum()) == int(nb.sum())   # every block counted once
+
+
+def test_loose_max_seq_len_keeps_a_short_batch_spread(lib):
+    """256 one-token sequences under max_seq_len 131073: the slot term comes
+    from the batch's own longest sequence, so no CTA holds more than a few
+    pairs (a term from max_seq_len would put all 256 in one CTA)."""
+    L = vq.make_layout(num_q_heads=4, num_kv_heads=1)
+    s = vq.vq_default_num_splits(L, 256, 131073, 152)
+    assert vq.vq_decode_units_balanced(L, 256, 131073, 0, 152) == 1
+    units, pieces, _, _, _ = _assign(np.ones(256, dtype=np.int64), 1, 131073, s, 152)
+    assert units.max() <= 3 and pieces.max() == 1

@@ -142,3 +142,17 @@ def test_balanced_matches_fixed_splits():
     assert gc.device_status() == 0
     assert np.max(np.abs(fixed - bal)) < 1e-3
     _check(w, cal, refs, q, bal, lens, int(lens.max()), "balanced cfg2-reduced")
+
+
+@pytest.mark.parametrize("splits", [0, 2])
+def test_balanced_loose_max_seq_len(splits):
+    """max_seq_len far above the real lengths: the per-CTA range comes from the
+    batch's own longest sequence, and the outputs still match the oracle."""
+    w = W.custom(name="bal-loose", batch=6, num_q_heads=8, num_kv_heads=2, context=900, k_sub=4,
+                 v_sub=4, page_size=64)
+    lens = np.array([17, 200, 0, 65, 1, 130])
+    cal, gc, refs = _filled(w, lens)
+    q = W.queries(w)
+    got = _decode(gc, q, lens, 901, splits)
+    assert gc.device_status() == 0
+    _check(w, cal, refs, q, got, lens, 901, f"loose splits={splits}")
