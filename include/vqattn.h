@@ -223,11 +223,10 @@ int32_t vq_decode_units_balanced(const vq_layout* layout, int32_t batch, int32_t
  *   seq_lens     int32 [batch]: tokens each query attends to (cached plus
  *                appended); 0 gives a zero output row.
  *   max_seq_len  host upper bound of seq_lens, used to size the split grid;
- *                tokens beyond it are ignored.  Keep it tight: with two or
- *                more sequences it also bounds how few SMs one sequence's
- *                blocks may be spread over (about blocks(max_seq_len) /
- *                (num_splits - 1) blocks per SM at least), so a bound far
- *                above the real lengths crowds a short batch onto few SMs.
+ *                tokens beyond it are ignored.  With one sequence (fixed
+ *                splits) the split boundaries are fractions of it, so a tight
+ *                bound spreads the work best; with two or more the kernel
+ *                divides the batch's actual blocks.
  *   softmax_scale multiplies the scores; 0 selects 1/sqrt(D).
  *   num_splits   partials per (sequence, KV head); <= 0 selects the
  *                library's choice.  With one sequence (or num_splits 1) each
